@@ -1,0 +1,472 @@
+"""Benchmark of the DiT elementwise hot path on B300.
+
+One step = one pass of the whole path over one layer's synthetic tensors:
+  rope_cos_sin_precompute (the per-forward tables)
+  rope_rotate_half on q, rope_rotate_half on k
+  gelu_and_mul (GEGLU)
+  rmsnorm_residual twice (the pre-attention and pre-FFN norms of a Pre-Norm layer)
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload video]
+    python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
+
+Prints one JSON line.  `value` is the aggregate algorithmic HBM throughput
+(GB/s: bytes each op must move, summed over the step and all ranks, over the
+device time of the K timed steps, max over ranks).  Inputs are resident in HBM
+before timing; every kernel's inputs exceed the 126 MB L2 except the cos/sin
+tables, which the step itself produces and the two RoPE calls consume.
+Multi-rank runs (torchrun) are independent replicas of the same layer (weak
+scaling); the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+PKG = "diffusion_transformer_elementwise_rotate_b300"
+METRIC = "fused RoPE/GEGLU/RMSNorm HBM GB/s and % of B300 peak; Mtokens/s per layer"
+FALLBACK_HBM_GBS = 6400.0
+OPS = ["rope_cos_sin_precompute", "rope_rotate_half_q", "rope_rotate_half_k", "gelu_and_mul",
+       "rmsnorm_residual_attn", "rmsnorm_residual_ffn"]
+DOMINANT = "gelu_and_mul"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="video")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(wl, W):
+    b = W.algorithmic_bytes(wl)
+    return {
+        "rope_cos_sin_precompute": b["rope_cos_sin_precompute"],
+        "rope_rotate_half_q": b["rope_rotate_half"],
+        "rope_rotate_half_k": b["rope_rotate_half"],
+        "gelu_and_mul": b["gelu_and_mul"],
+        "rmsnorm_residual_attn": b["rmsnorm_residual"],
+        "rmsnorm_residual_ffn": b["rmsnorm_residual"],
+    }
+
+
+def source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, PKG, "csrc", name), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def recorded_traffic(wl_name: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, if it was taken on the current source of that kernel."""
+    path = os.path.join(ROOT, "profiles", "gelu_and_mul_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    if d.get("source_sha256_16") != source_hash("gelu_and_mul.cu"):
+        return None
+    per = d.get("per_workload", {}).get(wl_name)
+    return None if per is None else float(per["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.file.read().splitlines() if ln.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ native arm
+
+class Layer:
+    """One layer's tensors on the device plus pinned host copies."""
+
+    def __init__(self, wl, W, dev):
+        self.wl = wl
+        pin = torch.cuda.is_available()
+        self.h_in = {
+            "freqs": W.freqs_for(wl).pin_memory() if pin else W.freqs_for(wl),
+            "q": W.rope_inputs(wl, "q", pin=pin),
+            "k": W.rope_inputs(wl, "k", pin=pin),
+            "gate_up": W.geglu_inputs(wl, pin=pin),
+        }
+        x1, r1, w = W.rmsnorm_inputs(wl, False, pin=pin)
+        x2, r2, _ = W.rmsnorm_inputs(wl, True, pin=pin)
+        self.h_in.update({"x1": x1, "r1": r1, "x2": x2, "r2": r2, "w": w})
+        self.d = {k: v.to(dev) for k, v in self.h_in.items()}
+        B, S, H, D, F, T, C = wl.B, wl.S, wl.H, wl.D, wl.F, wl.T_norm, wl.C
+        e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)  # noqa: E731
+        self.d.update({"cos": e((B * S, wl.rot)), "sin": e((B * S, wl.rot)),
+                       "q_out": e((B, S, H, D)), "k_out": e((B, S, H, D)),
+                       "ff_out": e((wl.T_ff, F)), "y1": e((T, C)), "y2": e((T, C))})
+        self.out_names = ["cos", "sin", "q_out", "k_out", "ff_out", "y1", "y2", "r1", "r2"]
+        self.h_out = {n: torch.empty(self.d[n].shape, dtype=self.d[n].dtype, pin_memory=pin)
+                      for n in self.out_names}
+
+    def step(self, dt, ev=None):
+        d, F = self.d, self.wl.F
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record()
+
+        mark(0)
+        dt.rope_cos_sin_precompute(d["freqs"], d["cos"], d["sin"])
+        mark(1)
+        dt.rope_rotate_half(d["q"], d["cos"], d["sin"], out=d["q_out"])
+        mark(2)
+        dt.rope_rotate_half(d["k"], d["cos"], d["sin"], out=d["k_out"])
+        mark(3)
+        dt.gelu_and_mul(d["gate_up"][:, :F], d["gate_up"][:, F:], out=d["ff_out"])
+        mark(4)
+        dt.rmsnorm_residual(d["x1"], d["r1"], d["w"], 1e-6, out=d["y1"])
+        mark(5)
+        dt.rmsnorm_residual(d["x2"], d["r2"], d["w"], 1e-6, out=d["y2"])
+        mark(6)
+
+    def h2d(self):
+        for k, v in self.h_in.items():
+            self.d[k].copy_(v, non_blocking=True)
+        return sum(v.numel() * v.element_size() for v in self.h_in.values())
+
+    def d2h(self):
+        for k in self.out_names:
+            self.h_out[k].copy_(self.d[k], non_blocking=True)
+        return sum(self.h_out[k].numel() * self.h_out[k].element_size() for k in self.out_names)
+
+
+def cpu_baseline(wl, W, layer, target_s=15.0):
+    """Time the oracle (as it stands, all host cores it uses) on a bounded
+    sample of the same workload: the first `frac` of each op's rows."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import oracle
+    h = layer.h_in
+    bts = step_bytes(wl, W)
+    total_bytes = sum(bts.values())
+
+    def run(frac):
+        tok = max(1, int(wl.S * frac))
+        rows_ff = max(1, int(wl.T_ff * frac))
+        rows_n = max(1, int(wl.T_norm * frac))
+        F = wl.F
+        freqs = h["freqs"][:tok].numpy()
+        q = oracle.bf16_bits(h["q"][:, :tok])
+        k = oracle.bf16_bits(h["k"][:, :tok])
+        gu = oracle.bf16_bits(h["gate_up"][:rows_ff])
+        x1, r1 = oracle.bf16_bits(h["x1"][:rows_n]), oracle.bf16_bits(h["r1"][:rows_n])
+        x2, r2 = oracle.bf16_bits(h["x2"][:rows_n]), oracle.bf16_bits(h["r2"][:rows_n])
+        w = oracle.bf16_bits(h["w"])
+        t0 = time.perf_counter()
+        c, s = oracle.rope_cos_sin(freqs)
+        oracle.rope_rotate_half(q, c, s)
+        oracle.rope_rotate_half(k, c, s)
+        oracle.gelu_and_mul(gu[:, :F], gu[:, F:])
+        oracle.rmsnorm_residual(x1, r1, w, 1e-6)
+        oracle.rmsnorm_residual(x2, r2, w, 1e-6)
+        dt_s = time.perf_counter() - t0
+        sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S
+                   + 2 * bts["rope_rotate_half_q"] * tok / wl.S
+                   + bts["gelu_and_mul"] * rows_ff / wl.T_ff
+                   + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
+        return dt_s, sampled, (tok, rows_ff, rows_n)
+
+    t, _, _ = run(1.0 / 2048)  # calibration
+    frac = min(1.0, (1.0 / 2048) * target_s / max(t, 1e-3))
+    t, sampled, (tok, rf, rn) = run(frac)
+    return {"value": round(sampled / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": (f"{wl.name} layer: first {tok} of {wl.S} tokens for the tables and q/k "
+                       f"RoPE, first {rf} of {wl.T_ff} GEGLU rows, first {rn} of {wl.T_norm} "
+                       f"rows for each RMSNorm; {sampled / 1e9:.3f} GB of algorithmic traffic "
+                       f"in {t:.2f} s"),
+            "fraction_of_step": round(sampled / total_bytes, 6)}
+
+
+def native(args):
+    sys.path.insert(0, ROOT)
+    import importlib
+    dt = importlib.import_module(PKG)
+    W = importlib.import_module(PKG + ".workloads")
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+        pg = tdist
+    dt.load()
+    wl = W.WORKLOADS[args.workload]
+    layer = Layer(wl, W, dev)
+    bts = step_bytes(wl, W)
+    per_step = sum(bts.values())
+
+    for _ in range(max(3, args.warmup)):
+        layer.step(dt)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        layer.step(dt, evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+               for j, op in enumerate(OPS)}
+    if pg:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / K
+    value = per_step * world * K / (elapsed_ms / 1e3) / 1e9
+
+    # end to end through host buffers: H2D inputs, the step, D2H outputs
+    KE = max(1, args.e2e_steps)
+    layer.h2d()
+    layer.step(dt)
+    layer.d2h()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(KE):
+        hb = layer.h2d()
+        layer.step(dt)
+        db = layer.d2h()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = per_step * world * KE / (e2e_ms / 1e3) / 1e9
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    peak, peak_kind = peaks()
+    dom_ms = kern_ms[DOMINANT]
+    achieved = bts[DOMINANT] / (dom_ms / 1e3) / 1e9
+    tokens = wl.B * wl.S
+    layer_ms = sum(kern_ms[o] for o in OPS[1:])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/gate/up/x, N(0,4) residual, N(1,0.1) w; "
+                "rotary angles from the token grid)",
+        "config": {
+            "workload": (f"{wl.name} DiT layer: q,k ({wl.B},{wl.S},{wl.H},{wl.D}) rot {wl.rot} "
+                         f"split {'/'.join(map(str, wl.split))}; GEGLU ({wl.T_ff}, 2x{wl.F}); "
+                         f"RMSNorm+residual ({wl.T_norm}, {wl.C}) x2; cos/sin tables "
+                         f"({wl.tokens}, {wl.rot})"),
+            "step": "tables + RoPE q + RoPE k + GEGLU + 2x RMSNorm+residual",
+            "bytes_per_step": per_step,
+            "l2": "inputs larger than L2 (126 MB) for every kernel; no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "mtokens_per_s_per_layer": round(tokens / (layer_ms / 1e3) / 1e6, 3),
+        "kernels": {op: {"ms": round(kern_ms[op], 5), "bytes": bts[op],
+                         "gbs": round(bts[op] / (kern_ms[op] / 1e3) / 1e9, 1)} for op in OPS},
+        "roofline": {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
+                     "algorithmic_bytes": bts[DOMINANT]},
+        "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": hb,
+                "d2h_bytes_per_step": db, "steps": KE},
+        "gpu_launches": 6 * K,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, W, layer)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def reference(args):
+    """The CPU oracle timed on host cores on the same workload and metric; each
+    step runs a bounded sample of the layer (a fixed slice of every op's rows)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    sys.path.insert(0, ROOT)
+    import importlib
+    W = importlib.import_module(PKG + ".workloads")
+    import oracle
+    wl = W.WORKLOADS[args.workload]
+    bts = step_bytes(wl, W)
+    steps, warm = args.steps, max(3, args.warmup)
+    # rows per step sized so the whole run stays within a couple of minutes
+    budget_s = 120.0
+    tok = max(1, wl.S // 4096)
+    rows_ff = max(1, wl.T_ff // 8192)
+    rows_n = max(1, wl.T_norm // 4096)
+    F = wl.F
+    freqs = W.freqs_for(wl)[:tok].numpy()
+    q = oracle.bf16_bits(W.normal_bf16((wl.B, tok, wl.H, wl.D), wl.seed, 0))
+    k = oracle.bf16_bits(W.normal_bf16((wl.B, tok, wl.H, wl.D), wl.seed, 1))
+    gu = oracle.bf16_bits(W.normal_bf16((rows_ff, 2 * F), wl.seed, 2))
+    x = oracle.bf16_bits(W.normal_bf16((rows_n, wl.C), wl.seed, 4))
+    r = oracle.bf16_bits(W.normal_bf16((rows_n, wl.C), wl.seed, 5, std=2.0))
+    w = oracle.bf16_bits(W.normal_bf16((wl.C,), wl.seed, 6, mean=1.0, std=math.sqrt(0.1)))
+    sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S + 2 * bts["rope_rotate_half_q"] * tok / wl.S
+               + bts["gelu_and_mul"] * rows_ff / wl.T_ff + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
+
+    def one():
+        c, s = oracle.rope_cos_sin(freqs)
+        oracle.rope_rotate_half(q, c, s)
+        oracle.rope_rotate_half(k, c, s)
+        oracle.gelu_and_mul(gu[:, :F], gu[:, F:])
+        oracle.rmsnorm_residual(x, r, w, 1e-6)
+        oracle.rmsnorm_residual(x, r, w, 1e-6)
+
+    t0 = time.perf_counter()
+    one()
+    per = time.perf_counter() - t0
+    if per * (steps + warm) > budget_s:
+        steps = max(1, int(budget_s / per) - warm)
+    for _ in range(warm):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    el = time.perf_counter() - t0
+    value = sampled * steps / el / 1e9
+    sample = (f"{wl.name} layer, per step: {tok} tokens of tables and q/k RoPE, {rows_ff} GEGLU "
+              f"rows, {rows_n} rows for each RMSNorm ({sampled / 1e6:.2f} MB algorithmic)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": round(1e3 * el / steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (emulated in fp64)", "data": "synthetic",
+        "config": {"workload": f"{wl.name} DiT layer (bounded sample per step)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,10 @@
-"""B300-native elementwise hot path of a diffusion-transformer block."""
+"""B300-native elementwise hot path of a diffusion-transformer block.
+
+Four ops, each one sm_103a CUDA kernel behind the C ABI in include/dtrot.h:
+rotary cos/sin tables, rotate-half RoPE, GEGLU with activation rounding, and
+RMSNorm fused with the residual add.  The torch wrappers in `api` only pass
+pointers, sizes and strides; `_capi` is the raw ctypes binding.
+"""
+from ._capi import DtrotError, DtrotUnavailable, load  # noqa: F401
+from .api import (gelu_and_mul, gelu_and_mul_fused, rmsnorm_residual,  # noqa: F401
+                  rope_cos_sin_precompute, rope_rotate_half)

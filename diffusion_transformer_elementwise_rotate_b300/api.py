@@ -1,0 +1,147 @@
+"""torch-tensor front end of the C ABI (argument marshalling only).
+
+Every function takes CUDA tensors on the current device, passes their data
+pointers, sizes and element strides to the matching `dtrot_*` entry point, and
+enqueues the kernel on torch's current stream of that device.  All arithmetic
+runs in libdtrot's sm_103a kernels.
+
+  rope_cos_sin_precompute(freqs)         -> (cos, sin)   ERNIE-Image page, section 1
+  rope_rotate_half(x, cos, sin, out=None) -> out         ERNIE-Image page, section 2
+  gelu_and_mul(gate, up, out=None)        -> out         ERNIE-Image page, section 3
+  gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
+  rmsnorm_residual(x, residual, w, eps=1e-6, out=None) -> out   (residual updated in place)
+                                                         sequence-parallelism post
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _capi
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _last_contiguous(t: torch.Tensor, name: str) -> None:
+    if t.dim() and t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+
+
+def rope_cos_sin_precompute(freqs: torch.Tensor, cos_out: torch.Tensor | None = None,
+                            sin_out: torch.Tensor | None = None):
+    """freqs fp32 (S, B, 1, R) -> cos, sin bf16 (B*S, R)."""
+    _need(freqs, "freqs", torch.float32)
+    if freqs.dim() != 4 or freqs.shape[2] != 1:
+        raise ValueError("freqs must be (S, B, 1, R)")
+    if not freqs.is_contiguous():
+        raise ValueError("freqs must be contiguous")
+    S, B, _, R = freqs.shape
+    if cos_out is None:
+        cos_out = torch.empty((B * S, R), dtype=torch.bfloat16, device=freqs.device)
+    if sin_out is None:
+        sin_out = torch.empty((B * S, R), dtype=torch.bfloat16, device=freqs.device)
+    for t, n in ((cos_out, "cos_out"), (sin_out, "sin_out")):
+        _need(t, n, torch.bfloat16)
+        if t.shape != (B * S, R) or not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous (B*S, R)")
+    _capi.check("dtrot_rope_cos_sin_precompute", freqs.data_ptr(), S, B, R, cos_out.data_ptr(),
+                sin_out.data_ptr(), _stream(freqs))
+    return cos_out, sin_out
+
+
+def rope_rotate_half(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """x bf16 (B, S, H, D) (any strides, D contiguous); cos/sin bf16 (B*S, rot)."""
+    _need(x, "x", torch.bfloat16)
+    _need(cos, "cos", torch.bfloat16)
+    _need(sin, "sin", torch.bfloat16)
+    if x.dim() != 4:
+        raise ValueError("x must be (B, S, H, D)")
+    _last_contiguous(x, "x")
+    B, S, H, D = x.shape
+    if cos.dim() != 2 or cos.shape != sin.shape or cos.shape[0] != B * S:
+        raise ValueError("cos/sin must be (B*S, rot_dim)")
+    if not (cos.is_contiguous() and sin.is_contiguous()):
+        raise ValueError("cos/sin must be contiguous")
+    rot = cos.shape[1]
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16)
+    if out.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    _last_contiguous(out, "out")
+    sx, so = x.stride(), out.stride()
+    _capi.check("dtrot_rope_rotate_half", x.data_ptr(), B, S, H, D, sx[0], sx[1], sx[2],
+                cos.data_ptr(), sin.data_ptr(), rot, out.data_ptr(), so[0], so[1], so[2],
+                _stream(x))
+    return out
+
+
+def _rows(t: torch.Tensor, name: str):
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D (rows, features)")
+    _last_contiguous(t, name)
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """gate, up bf16 (T, F) (row strides allowed) -> out bf16 (T, F)."""
+    _need(gate, "gate", torch.bfloat16)
+    _need(up, "up", torch.bfloat16)
+    if gate.shape != up.shape:
+        raise ValueError("gate and up must have the same shape")
+    T, F = gate.shape
+    sg, su = _rows(gate, "gate"), _rows(up, "up")
+    if out is None:
+        out = torch.empty((T, F), dtype=torch.bfloat16, device=gate.device)
+    _need(out, "out", torch.bfloat16)
+    if out.shape != gate.shape:
+        raise ValueError("out must be (T, F)")
+    so = _rows(out, "out")
+    _capi.check("dtrot_gelu_and_mul", gate.data_ptr(), sg, up.data_ptr(), su, out.data_ptr(),
+                so, T, F, _stream(gate))
+    return out
+
+
+def gelu_and_mul_fused(gate_up: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """(..., 2F) buffer, gate = [..., :F], up = [..., F:] -> (..., F)."""
+    if gate_up.shape[-1] % 2:
+        raise ValueError("the last dimension of gate_up must be even")
+    F = gate_up.shape[-1] // 2
+    g2 = gate_up.reshape(-1, 2 * F)
+    o2 = None if out is None else out.view(-1, F)
+    r = gelu_and_mul(g2[:, :F], g2[:, F:], o2)
+    return r.view(*gate_up.shape[:-1], F)
+
+
+def rmsnorm_residual(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor,
+                     eps: float = 1e-6, out: torch.Tensor | None = None) -> torch.Tensor:
+    """x, residual bf16 (T, C); w bf16 (C,).  residual is overwritten with
+    h = x + residual; returns out = RMSNorm(h) * w."""
+    _need(x, "x", torch.bfloat16)
+    _need(residual, "residual", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    if x.shape != residual.shape or w.dim() != 1 or w.shape[0] != x.shape[-1]:
+        raise ValueError("shapes: x (T, C), residual (T, C), w (C,)")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    T, C = x.shape
+    sx, sr = _rows(x, "x"), _rows(residual, "residual")
+    if out is None:
+        out = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16)
+    so = _rows(out, "out")
+    _capi.check("dtrot_rmsnorm_residual", x.data_ptr(), sx, residual.data_ptr(), sr,
+                w.data_ptr(), float(eps), out.data_ptr(), so, T, C, _stream(x))
+    return out

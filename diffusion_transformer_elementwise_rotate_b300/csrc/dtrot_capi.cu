@@ -1,0 +1,312 @@
+// extern "C" entry points of libdtrot: host-side argument validation, then one
+// kernel launch on the caller's stream.  The declarations, with the meaning,
+// layout, ownership and error behaviour of every argument, are in dtrot.h.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dtrot.h"
+#include "dtrot_internal.cuh"
+
+#define DTROT_API extern "C" __attribute__((visibility("default")))
+
+namespace dtrot {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_arch_ok[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev;
+}
+
+bool device_ok() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    int st = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        g_sms[dev].store(sms, std::memory_order_relaxed);
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        g_arch_ok[dev].store(st, std::memory_order_relaxed);
+    }
+    return st == 1;
+}
+
+// ---- shape / stride / overlap helpers (element counts, int64) ----
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+
+// Byte range [lo, hi) touched by a strided view with positive strides.
+struct Range {
+    uintptr_t lo, hi;
+};
+
+bool span(const void* base, int elem, const int64_t* size, const int64_t* stride, int n,
+          Range* r) {
+    int64_t last = 0;
+    for (int i = 0; i < n; ++i) {
+        int64_t t;
+        if (!mul_ok(size[i] - 1, stride[i], &t)) return false;
+        if (__builtin_add_overflow(last, t, &last)) return false;
+    }
+    int64_t bytes;
+    if (!mul_ok(last + 1, elem, &bytes)) return false;
+    r->lo = (uintptr_t)base;
+    r->hi = r->lo + (uintptr_t)bytes;
+    return true;
+}
+
+bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// True if no two distinct index tuples of the view share an element.
+bool non_self_overlapping(const int64_t* size, const int64_t* stride, int n) {
+    int idx[8];
+    int m = 0;
+    for (int i = 0; i < n; ++i)
+        if (size[i] > 1) idx[m++] = i;
+    std::sort(idx, idx + m, [&](int a, int b) { return stride[a] < stride[b]; });
+    int64_t extent = 0;  // elements spanned by the dims already placed, minus one
+    for (int k = 0; k < m; ++k) {
+        const int i = idx[k];
+        if (stride[i] <= extent) return false;
+        int64_t t;
+        if (!mul_ok(size[i] - 1, stride[i], &t)) return false;
+        extent += t;
+    }
+    return true;
+}
+
+// Two (rows, cols) views with row strides sa, sb: element-disjoint?
+bool views2d_disjoint(const uint16_t* a, int64_t sa, const uint16_t* b, int64_t sb,
+                      int64_t rows, int64_t cols) {
+    int64_t sz[2] = {rows, cols};
+    int64_t st_a[2] = {sa, 1}, st_b[2] = {sb, 1};
+    Range ra, rb;
+    if (!span(a, 2, sz, st_a, 2, &ra) || !span(b, 2, sz, st_b, 2, &rb)) return false;
+    if (!overlap(ra, rb)) return true;
+    if (sa != sb || rows == 1) return false;
+    const intptr_t dbytes = (intptr_t)((uintptr_t)b - (uintptr_t)a);
+    if (dbytes % 2) return false;
+    const int64_t d = (int64_t)(dbytes / 2);
+    const int64_t m = ((d % sa) + sa) % sa;
+    return m >= cols && m <= sa - cols;
+}
+
+// A single row [w, w + cols) against a (rows, cols) view with row stride sv.
+// Disjoint if the byte ranges are, or if w's offset from the view, taken
+// modulo sv, falls in a gap between rows (checked on w repeated every sv).
+bool row_disjoint(const uint16_t* w, int64_t cols, const uint16_t* v, int64_t sv,
+                  int64_t rows) {
+    int64_t sz[2] = {rows, cols}, st[2] = {sv, 1};
+    Range rv;
+    if (!span(v, 2, sz, st, 2, &rv)) return false;
+    const Range rw{(uintptr_t)w, (uintptr_t)w + (uintptr_t)cols * 2};
+    if (!overlap(rw, rv)) return true;
+    return views2d_disjoint(v, sv, w, sv, rows, cols);
+}
+
+dtrot_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return DTROT_OK;
+    return DTROT_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    int s = g_sms[dev].load(std::memory_order_relaxed);
+    if (s <= 0) {
+        if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            s = 148;
+        }
+        g_sms[dev].store(s, std::memory_order_relaxed);
+    }
+    return s;
+}
+
+}  // namespace dtrot
+
+using namespace dtrot;
+
+DTROT_API const char* dtrot_status_str(dtrot_status s) {
+    switch (s) {
+        case DTROT_OK: return "DTROT_OK";
+        case DTROT_ERR_NULL: return "DTROT_ERR_NULL: a required pointer is NULL";
+        case DTROT_ERR_SHAPE: return "DTROT_ERR_SHAPE: a size is negative or too large";
+        case DTROT_ERR_ROTDIM: return "DTROT_ERR_ROTDIM: rot_dim must be even, > 0 and <= D";
+        case DTROT_ERR_STRIDE: return "DTROT_ERR_STRIDE: a stride is invalid";
+        case DTROT_ERR_ALIAS: return "DTROT_ERR_ALIAS: an output overlaps an input";
+        case DTROT_ERR_LAUNCH: return "DTROT_ERR_LAUNCH: the CUDA launch failed";
+        case DTROT_ERR_DEVICE: return "DTROT_ERR_DEVICE: no sm_103 CUDA device is current";
+        case DTROT_ERR_VALUE: return "DTROT_ERR_VALUE: a scalar argument is out of range";
+    }
+    return "DTROT_ERR_UNKNOWN";
+}
+
+DTROT_API int dtrot_version(void) { return 100; }  // 0.1.0
+
+DTROT_API dtrot_status dtrot_rope_cos_sin_precompute(const float* freqs, int64_t S, int64_t B,
+                                                     int64_t R, uint16_t* cos_out,
+                                                     uint16_t* sin_out, void* stream) {
+    if (S < 0 || B < 0 || R < 0) return DTROT_ERR_SHAPE;
+    int64_t n, n2;
+    if (!mul_ok(S, B, &n) || !mul_ok(n, R, &n) || !mul_ok(n, 8, &n2)) return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!freqs || !cos_out || !sin_out) return DTROT_ERR_NULL;
+    const Range rf{(uintptr_t)freqs, (uintptr_t)freqs + (uintptr_t)n * 4};
+    const Range rc{(uintptr_t)cos_out, (uintptr_t)cos_out + (uintptr_t)n * 2};
+    const Range rs{(uintptr_t)sin_out, (uintptr_t)sin_out + (uintptr_t)n * 2};
+    if (overlap(rc, rs) || overlap(rc, rf) || overlap(rs, rf)) return DTROT_ERR_ALIAS;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    return launch_status(
+        launch_rope_cos_sin(freqs, S, B, R, cos_out, sin_out, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int64_t S,
+                                              int64_t H, int64_t D, int64_t sx_b,
+                                              int64_t sx_s, int64_t sx_h, const uint16_t* cos,
+                                              const uint16_t* sin, int64_t rot_dim,
+                                              uint16_t* out, int64_t so_b, int64_t so_s,
+                                              int64_t so_h, void* stream) {
+    if (B < 0 || S < 0 || H < 0 || D < 0) return DTROT_ERR_SHAPE;
+    int64_t ntok, n;
+    if (!mul_ok(B, S, &ntok) || !mul_ok(ntok, H, &n) || !mul_ok(n, D, &n) ||
+        !mul_ok(n, 16, &n))
+        return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!x || !cos || !sin || !out) return DTROT_ERR_NULL;
+    if (rot_dim <= 0 || rot_dim % 2 || rot_dim > D) return DTROT_ERR_ROTDIM;
+    int64_t tab;
+    if (!mul_ok(ntok, rot_dim, &tab)) return DTROT_ERR_SHAPE;
+    const int64_t size[4] = {B, S, H, D};
+    const int64_t sxs[4] = {sx_b, sx_s, sx_h, 1};
+    const int64_t sos[4] = {so_b, so_s, so_h, 1};
+    for (int i = 0; i < 3; ++i)
+        if ((size[i] > 1 && (sxs[i] <= 0 || sos[i] <= 0)) || sxs[i] < 0 || sos[i] < 0)
+            return DTROT_ERR_STRIDE;
+    if (!non_self_overlapping(size, sos, 4)) return DTROT_ERR_STRIDE;
+    Range rx, ro;
+    if (!span(x, 2, size, sxs, 4, &rx) || !span(out, 2, size, sos, 4, &ro)) return DTROT_ERR_SHAPE;
+    const Range rc{(uintptr_t)cos, (uintptr_t)cos + (uintptr_t)tab * 2};
+    const Range rs{(uintptr_t)sin, (uintptr_t)sin + (uintptr_t)tab * 2};
+    bool in_place = false;
+    if (overlap(rx, ro)) {
+        bool same = (x == out);
+        for (int i = 0; i < 3; ++i)
+            if (size[i] > 1 && sxs[i] != sos[i]) same = false;
+        if (!same) return DTROT_ERR_ALIAS;
+        in_place = true;
+    }
+    if (overlap(ro, rc) || overlap(ro, rs)) return DTROT_ERR_ALIAS;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    RopeParams p;
+    p.x = x;
+    p.out = out;
+    p.cos = cos;
+    p.sin = sin;
+    p.B = B;
+    p.S = S;
+    p.H = H;
+    p.D = D;
+    p.rot = rot_dim;
+    p.sx_b = sx_b;
+    p.sx_s = sx_s;
+    p.sx_h = sx_h;
+    p.so_b = so_b;
+    p.so_s = so_s;
+    p.so_h = so_h;
+    p.in_place = in_place ? 1 : 0;
+    return launch_status(launch_rope_rotate_half(p, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
+                                          const uint16_t* up, int64_t s_up, uint16_t* out,
+                                          int64_t s_out, int64_t T, int64_t F, void* stream) {
+    if (T < 0 || F < 0) return DTROT_ERR_SHAPE;
+    int64_t n;
+    if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!gate || !up || !out) return DTROT_ERR_NULL;
+    if (T > 1 && (s_gate < F || s_up < F || s_out < F)) return DTROT_ERR_STRIDE;
+    if (s_gate < 0 || s_up < 0 || s_out < 0) return DTROT_ERR_STRIDE;
+    const int64_t sg = T > 1 ? s_gate : F, su = T > 1 ? s_up : F, so = T > 1 ? s_out : F;
+    {
+        int64_t size[2] = {T, F}, a[2] = {sg, 1}, b[2] = {su, 1}, c[2] = {so, 1};
+        Range r;
+        if (!span(gate, 2, size, a, 2, &r) || !span(up, 2, size, b, 2, &r) ||
+            !span(out, 2, size, c, 2, &r))
+            return DTROT_ERR_SHAPE;
+    }
+    const bool in_place = (out == gate) && (so == sg);
+    if (!in_place && !views2d_disjoint(out, so, gate, sg, T, F)) return DTROT_ERR_ALIAS;
+    if (!views2d_disjoint(out, so, up, su, T, F)) return DTROT_ERR_ALIAS;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    GegluParams p;
+    p.gate = gate;
+    p.up = up;
+    p.out = out;
+    p.s_gate = sg;
+    p.s_up = su;
+    p.s_out = so;
+    p.T = T;
+    p.F = F;
+    return launch_status(launch_gelu_and_mul(p, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_rmsnorm_residual(const uint16_t* x, int64_t sx, uint16_t* residual,
+                                              int64_t sr, const uint16_t* w, float eps,
+                                              uint16_t* out, int64_t so, int64_t T, int64_t C,
+                                              void* stream) {
+    if (T < 0 || C < 0) return DTROT_ERR_SHAPE;
+    int64_t n;
+    if (!mul_ok(T, C, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!x || !residual || !w || !out) return DTROT_ERR_NULL;
+    if (!(eps >= 0.0f) || !(eps <= 3.4028235e38f)) return DTROT_ERR_VALUE;
+    if (T > 1 && (sx < C || sr < C || so < C)) return DTROT_ERR_STRIDE;
+    if (sx < 0 || sr < 0 || so < 0) return DTROT_ERR_STRIDE;
+    const int64_t ssx = T > 1 ? sx : C, ssr = T > 1 ? sr : C, sso = T > 1 ? so : C;
+    {
+        int64_t size[2] = {T, C}, a[2] = {ssx, 1}, b[2] = {ssr, 1}, c[2] = {sso, 1};
+        Range r;
+        if (!span(x, 2, size, a, 2, &r) || !span(residual, 2, size, b, 2, &r) ||
+            !span(out, 2, size, c, 2, &r))
+            return DTROT_ERR_SHAPE;
+    }
+    const bool x_is_res = (x == residual) && (ssx == ssr);
+    if (!x_is_res && !views2d_disjoint(x, ssx, residual, ssr, T, C)) return DTROT_ERR_ALIAS;
+    if (!views2d_disjoint(out, sso, x, ssx, T, C)) return DTROT_ERR_ALIAS;
+    if (!views2d_disjoint(out, sso, residual, ssr, T, C)) return DTROT_ERR_ALIAS;
+    if (!row_disjoint(w, C, residual, ssr, T) || !row_disjoint(w, C, out, sso, T))
+        return DTROT_ERR_ALIAS;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    RmsParams p;
+    p.x = x;
+    p.residual = residual;
+    p.w = w;
+    p.out = out;
+    p.sx = ssx;
+    p.sr = ssr;
+    p.so = sso;
+    p.T = T;
+    p.C = C;
+    p.eps = eps;
+    return launch_status(launch_rmsnorm_residual(p, (cudaStream_t)stream));
+}

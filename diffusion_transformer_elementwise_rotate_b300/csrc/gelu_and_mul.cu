@@ -1,0 +1,160 @@
+// GEGLU with the eager path's activation rounding:
+//   out = RN16(up * RN16(RN32(gelu(gate)))),  gelu(x) = x/2 * (1 + erf(x/sqrt 2)).
+//
+// ERNIE-Image fusion page (sglang PR #34306 analysis), section 3: up *
+// F.gelu(gate) made two full passes over the FFN intermediate; the fused op
+// does one, reproducing the bf16 rounding of the GELU output.
+//
+// Design.  gate is bf16, so the rounded activation g(gate) takes one of 65536
+// values.  Each CTA first tabulates g for every bf16 bit pattern in shared
+// memory (128 KB), then streams gate/up with 128-bit loads: per element one
+// shared-memory lookup and one bf16x2 multiply with .rn rounding.  The erf
+// arithmetic (tens of fp32 instructions per element, enough to make a direct
+// evaluation ALU-bound on this part) is paid 65536 times per CTA instead of
+// once per element, and the result is the exactly rounded GELU.
+//
+// Table entries: fp32 erfcf decides the rounding unless the fp32 value lies
+// within an error margin of a bf16 rounding midpoint (the margin grows with
+// erfc's condition number 2z^2 for z = -x/sqrt 2 > 0); those entries, and the
+// far negative tail x in (-20, -9) where the fp32 erfc result loses precision
+// to underflow, are recomputed in fp64 and rounded to fp32, then to bf16.
+#include <atomic>
+
+#include "dtrot_internal.cuh"
+
+namespace dtrot {
+namespace {
+
+constexpr int kTable = 1 << 16;
+constexpr int kThreads = 1024;
+
+__device__ uint16_t gelu_entry(uint32_t bits) {
+    const float x = __uint_as_float(bits << 16);
+    const float z = __fmul_rn(x, -0.70710678118654752440f);  // -x / sqrt 2
+    bool slow = (x < -9.0f) && (x > -20.0f);
+    float y = 0.0f;
+    if (!slow) {
+        const float e = erfcf(z);
+        y = __fmul_rn(__fmul_rn(0.5f, x), e);
+        const float zz = z > 0.0f ? fminf(z, 16.0f) : 0.0f;
+        const int margin = 8 + (int)(4.0f * zz * zz);
+        slow = ulps_to_bf16_midpoint(y) <= margin;
+    }
+    if (slow) {
+        const double xd = (double)x;
+        y = __double2float_rn(0.5 * xd * erfc(-xd * 0.70710678118654752440));
+    }
+    return rn16f(y);
+}
+
+__device__ __forceinline__ uint32_t lookup2(const uint16_t* tab, uint32_t g) {
+    const uint32_t lo = tab[g & 0xFFFFu];
+    const uint32_t hi = tab[g >> 16];
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint4 geglu_vec(const uint16_t* tab, uint4 g, uint4 u) {
+    uint4 o;
+    o.x = bmul2(u.x, lookup2(tab, g.x));
+    o.y = bmul2(u.y, lookup2(tab, g.y));
+    o.z = bmul2(u.z, lookup2(tab, g.z));
+    o.w = bmul2(u.w, lookup2(tab, g.w));
+    return o;
+}
+
+__device__ void build_table(uint16_t* tab) {
+    for (int i = threadIdx.x; i < kTable; i += blockDim.x) tab[i] = gelu_entry((uint32_t)i);
+    __syncthreads();
+}
+
+// Vector path: F % 8 == 0, strides % 8 == 0, pointers 16-byte aligned.
+// Items are (row, 8-column vector) pairs, U per thread per iteration with all
+// loads of an iteration issued before its stores (safe for out == gate).
+template <int U>
+__global__ void __launch_bounds__(kThreads, 1) geglu_vec_kernel(GegluParams p) {
+    extern __shared__ uint16_t tab[];
+    build_table(tab);
+    const uint32_t nv = (uint32_t)(p.F >> 3);
+    const int64_t items = p.T * (int64_t)nv;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < items;
+         i0 += stride * U) {
+        uint4 g[U], u[U];
+        int64_t row[U];
+        uint32_t col[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i < items) {
+                row[k] = i / nv;
+                col[k] = (uint32_t)(i - row[k] * nv) << 3;
+                g[k] = *reinterpret_cast<const uint4*>(p.gate + row[k] * p.s_gate + col[k]);
+                u[k] = *reinterpret_cast<const uint4*>(p.up + row[k] * p.s_up + col[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i < items) {
+                *reinterpret_cast<uint4*>(p.out + row[k] * p.s_out + col[k]) =
+                    geglu_vec(tab, g[k], u[k]);
+            }
+        }
+    }
+}
+
+// Scalar path for any alignment / width.
+__global__ void __launch_bounds__(kThreads, 1) geglu_scalar_kernel(GegluParams p) {
+    extern __shared__ uint16_t tab[];
+    build_table(tab);
+    const int64_t items = p.T * p.F;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / p.F;
+        const int64_t c = i - r * p.F;
+        const uint32_t g = p.gate[r * p.s_gate + c];
+        const uint32_t u = p.up[r * p.s_up + c];
+        p.out[r * p.s_out + c] = (uint16_t)bmul2(u, tab[g]);
+    }
+}
+
+bool aligned(const void* ptr, int bytes) { return ((uintptr_t)ptr % bytes) == 0; }
+
+constexpr int kMaxDev = 64;
+std::atomic<bool> g_attr[kMaxDev][2];  // dynamic shared memory attribute set, per device
+
+}  // namespace
+
+cudaError_t launch_gelu_and_mul(const GegluParams& p, cudaStream_t st) {
+    const size_t smem = kTable * sizeof(uint16_t);
+    const bool vec = (p.F % 8 == 0) && (p.s_gate % 8 == 0) && (p.s_up % 8 == 0) &&
+                     (p.s_out % 8 == 0) && aligned(p.gate, 16) && aligned(p.up, 16) &&
+                     aligned(p.out, 16);
+    const int sms = num_sms();
+    // One CTA per SM (the table takes 128 KB of shared memory); fewer when the
+    // tensor is small, so tiny calls do not tabulate on every SM.
+    const int64_t work = vec ? p.T * (p.F / 8) : p.T * p.F;
+    int64_t blocks = (work + kThreads - 1) / kThreads;
+    if (blocks > sms) blocks = sms;
+    if (blocks < 1) blocks = 1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    const int which = vec ? 0 : 1;
+    if (!g_attr[dev][which].load(std::memory_order_acquire)) {
+        e = vec ? cudaFuncSetAttribute(geglu_vec_kernel<4>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                : cudaFuncSetAttribute(geglu_scalar_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        g_attr[dev][which].store(true, std::memory_order_release);
+    }
+    if (vec)
+        geglu_vec_kernel<4><<<(unsigned)blocks, kThreads, smem, st>>>(p);
+    else
+        geglu_scalar_kernel<<<(unsigned)blocks, kThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dtrot

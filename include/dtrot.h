@@ -1,0 +1,155 @@
+/*
+ * dtrot.h — C ABI of the B300 (sm_103a) elementwise hot path of a
+ * diffusion-transformer block: rotary cos/sin tables, rotate-half RoPE,
+ * GEGLU with activation rounding, and RMSNorm fused with the residual add.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 tensors are passed as `uint16_t*` holding bfloat16 bit patterns;
+ *    fp32 tensors as `float*`.  All data pointers are DEVICE pointers
+ *    (cudaMalloc, a caching allocator, or managed memory) on the device that is
+ *    current when the call is made.
+ *  - Sizes and strides are int64_t counts of ELEMENTS (not bytes).  The last
+ *    dimension of every tensor is contiguous (stride 1).
+ *  - `stream` is a cudaStream_t passed as `void*`; NULL means the legacy
+ *    default stream.  Work is enqueued on it and the call returns without
+ *    synchronising.  The library allocates nothing, frees nothing and makes no
+ *    host-device synchronisation, so calls may be captured in a CUDA graph.
+ *  - The caller owns every buffer.  Outputs are fully overwritten; inputs are
+ *    only read, except `residual` of dtrot_rmsnorm_residual, which is updated.
+ *  - Any alignment is accepted.  Pointers and strides that are multiples of
+ *    8 elements (16 bytes) take 128-bit vector paths; others take narrower
+ *    vector or scalar paths with identical results.
+ *  - A call with a zero-sized dimension does nothing and returns DTROT_OK
+ *    (pointers may then be NULL).
+ *  - Arguments are validated on the host before anything is launched.  An
+ *    invalid call launches nothing and returns its status; a launch failure is
+ *    reported as DTROT_ERR_LAUNCH from cudaGetLastError().  No device-side
+ *    assert or trap is used.
+ *
+ * Rounding: RN16 is round-to-nearest-even to bfloat16 (8 significant bits,
+ * the fp32 exponent range, subnormals kept); RN32 likewise to fp32.
+ *
+ * Source pages (cited by title and section):
+ *  [P4] "[sglang] ERNIE-Image ... RoPE and GELU-mul fusion and RoPE cos/sin
+ *       hoisting" (analysis of sglang PR #34306), sections 1-3.
+ *  [P5] "SP: splitting activations alongside TP" (sequence-parallelism post),
+ *       section on per-token normalisation and residual add, and the Pre-Norm
+ *       layer figure.
+ */
+#ifndef DTROT_H
+#define DTROT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dtrot_status {
+    DTROT_OK = 0,
+    DTROT_ERR_NULL = 1,   /* a required pointer is NULL */
+    DTROT_ERR_SHAPE = 2,  /* a size is negative, or an element count overflows */
+    DTROT_ERR_ROTDIM = 3, /* rot_dim is odd, zero, or larger than D */
+    DTROT_ERR_STRIDE = 4, /* a stride is not positive, or rows/heads of an output overlap */
+    DTROT_ERR_ALIAS = 5,  /* an output overlaps an input in a way the call does not allow */
+    DTROT_ERR_LAUNCH = 6, /* the CUDA launch failed (see cudaGetLastError) */
+    DTROT_ERR_DEVICE = 7, /* no current CUDA device, or it is not sm_103 */
+    DTROT_ERR_VALUE = 8   /* a scalar argument is out of range (eps) */
+} dtrot_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* dtrot_status_str(dtrot_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dtrot_version(void);
+
+/*
+ * Rotary cos/sin tables, computed once per forward.            [P4] section 1
+ *
+ *   cos_out[b*S + s, j] = RN16(RN32(cos(freqs[s, b, 0, j])))
+ *   sin_out[b*S + s, j] = RN16(RN32(sin(freqs[s, b, 0, j])))
+ *
+ * i.e. the (S, B, 1, R) -> (B, S, 1, R) permute, cos/sin in fp32 and the cast
+ * to bf16, reshaped to (B*S, R) rows, with the fp32 cos/sin taken as correctly
+ * rounded.
+ *   freqs    fp32, (S, B, 1, R) contiguous, read only.
+ *   cos_out, sin_out  bf16, (B*S, R) contiguous, written.  They must not
+ *            overlap each other or freqs (DTROT_ERR_ALIAS).
+ */
+dtrot_status dtrot_rope_cos_sin_precompute(const float* freqs, int64_t S, int64_t B,
+                                           int64_t R, uint16_t* cos_out,
+                                           uint16_t* sin_out, void* stream);
+
+/*
+ * Rotate-half RoPE over the leading rot_dim columns of x.      [P4] section 2
+ *
+ * With h = rot_dim / 2 and c, s = row b*S + s of cos/sin (shared by all H
+ * heads of that token), for every (b, s, head):
+ *   j <  h:          out[j] = RN16(RN16(x[j]*c[j]) + RN16(-x[j+h]*s[j]))
+ *   h <= j < rot_dim: out[j] = RN16(RN16(x[j]*c[j]) + RN16( x[j-h]*s[j]))
+ *   j >= rot_dim:    out[j] = x[j]        (tail columns pass through)
+ * which is the eager chunk / neg / cat / mul / add chain with its per-op bf16
+ * rounding, round(round(x1*cos1) + round(-x2*sin1)).
+ *   x        bf16, (B, S, H, D) with element strides (sx_b, sx_s, sx_h) and
+ *            the D axis contiguous, read only.
+ *   cos, sin bf16, (B*S, rot_dim) contiguous (from the call above).
+ *   rot_dim  even, 0 < rot_dim <= D (else DTROT_ERR_ROTDIM).
+ *   out      bf16, (B, S, H, D) with strides (so_b, so_s, so_h), written.
+ *            out == x with identical strides (in place) is allowed; any other
+ *            overlap with x, cos or sin is DTROT_ERR_ALIAS.  Distinct output
+ *            rows must not overlap (DTROT_ERR_STRIDE).  In place, the tail
+ *            columns are left untouched (they already hold x).
+ */
+dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int64_t S, int64_t H,
+                                    int64_t D, int64_t sx_b, int64_t sx_s, int64_t sx_h,
+                                    const uint16_t* cos, const uint16_t* sin,
+                                    int64_t rot_dim, uint16_t* out, int64_t so_b,
+                                    int64_t so_s, int64_t so_h, void* stream);
+
+/*
+ * GEGLU with the eager path's activation rounding.             [P4] section 3
+ *
+ *   out[t, f] = RN16(up[t, f] * RN16(RN32(gelu(gate[t, f]))))
+ *   gelu(x)   = x * 1/2 * (1 + erf(x / sqrt 2))    (exact, erf-based GELU)
+ *
+ * gelu(-inf) follows IEEE evaluation of the formula (-inf * 0 = NaN).
+ *   gate, up  bf16, (T, F), row strides s_gate, s_up >= F (elements), read
+ *             only.  They may be the two halves of one (T, 2F) buffer
+ *             (gate = columns [0, F), up = columns [F, 2F), strides 2F).
+ *   out       bf16, (T, F), row stride s_out >= F, written.  out == gate with
+ *             s_out == s_gate (in place) is allowed; any other element overlap
+ *             with gate or up is DTROT_ERR_ALIAS.
+ */
+dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate, const uint16_t* up,
+                                int64_t s_up, uint16_t* out, int64_t s_out, int64_t T,
+                                int64_t F, void* stream);
+
+/*
+ * Token-wise RMSNorm fused with the residual add (Pre-Norm).   [P5]
+ *
+ * For every token row t:
+ *   h[c]          = RN16(x[c] + residual[c])             (new residual stream)
+ *   residual[c]  := h[c]
+ *   out[c]        = RN16(h[c] * (mean_c(h^2) + eps)^(-1/2) * w[c])
+ * Each row uses only its own features, so any subset of rows gives the same
+ * values as the corresponding rows of the whole tensor.
+ *   x         bf16, (T, C), row stride sx >= C, read only.
+ *   residual  bf16, (T, C), row stride sr >= C, read and overwritten with h.
+ *             x == residual with sx == sr is allowed (h = RN16(2x)); any other
+ *             overlap of x and residual is DTROT_ERR_ALIAS.
+ *   w         bf16, (C), read only; must not overlap residual or out.
+ *   eps       finite and >= 0 (else DTROT_ERR_VALUE); added inside the root.
+ *   out       bf16, (T, C), row stride so >= C, written; must not overlap x,
+ *             residual or w.
+ */
+dtrot_status dtrot_rmsnorm_residual(const uint16_t* x, int64_t sx, uint16_t* residual,
+                                    int64_t sr, const uint16_t* w, float eps,
+                                    uint16_t* out, int64_t so, int64_t T, int64_t C,
+                                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTROT_H */

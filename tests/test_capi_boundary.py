@@ -1,0 +1,179 @@
+"""The C ABI boundary, on the host (no GPU needed).
+
+- libdtrot.so loads and exports every entry point include/dtrot.h declares;
+- every invalid argument returns its own status code before anything is
+  launched (the pointers used here are never dereferenced);
+- zero-sized calls are no-ops that return DTROT_OK.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from diffusion_transformer_elementwise_rotate_b300 import _capi
+from diffusion_transformer_elementwise_rotate_b300 import build as dbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dtrot.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dbuild.build()
+    return _capi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dtrot_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_ops():
+    names = declared_functions()
+    for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half", "dtrot_gelu_and_mul",
+               "dtrot_rmsnorm_residual", "dtrot_status_str", "dtrot_version"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _capi.SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_status_strings(lib):
+    for code, name in _capi.STATUS.items():
+        s = lib.dtrot_status_str(code).decode()
+        assert s.startswith(name)
+    assert lib.dtrot_version() >= 100
+
+
+P = 0x100000  # fake, 256-byte aligned device addresses (never dereferenced)
+Q = 0x900000
+R = 0x1100000
+W = 0x1900000
+
+
+def rope(**kw):
+    a = dict(x=P, B=1, S=4, H=2, D=8, sx_b=64, sx_s=16, sx_h=8, cos=Q, sin=R, rot=8, out=W,
+             so_b=64, so_s=16, so_h=8)
+    a.update(kw)
+    return _capi.call("dtrot_rope_rotate_half", a["x"], a["B"], a["S"], a["H"], a["D"],
+                      a["sx_b"], a["sx_s"], a["sx_h"], a["cos"], a["sin"], a["rot"], a["out"],
+                      a["so_b"], a["so_s"], a["so_h"], None)
+
+
+def geglu(**kw):
+    a = dict(gate=P, sg=16, up=P + 16, su=16, out=W, so=8, T=4, F=8)
+    a.update(kw)
+    return _capi.call("dtrot_gelu_and_mul", a["gate"], a["sg"], a["up"], a["su"], a["out"],
+                      a["so"], a["T"], a["F"], None)
+
+
+def rms(**kw):
+    a = dict(x=P, sx=8, res=Q, sr=8, w=R, eps=1e-6, out=W, so=8, T=4, C=8)
+    a.update(kw)
+    return _capi.call("dtrot_rmsnorm_residual", a["x"], a["sx"], a["res"], a["sr"], a["w"],
+                      a["eps"], a["out"], a["so"], a["T"], a["C"], None)
+
+
+def tables(**kw):
+    a = dict(f=P, S=4, B=2, R=8, c=Q, s=R)
+    a.update(kw)
+    return _capi.call("dtrot_rope_cos_sin_precompute", a["f"], a["S"], a["B"], a["R"], a["c"],
+                      a["s"], None)
+
+
+def test_zero_sized_calls_are_noops(lib):
+    assert rope(B=0, x=0, cos=0, sin=0, out=0) == _capi.OK
+    assert rope(H=0) == _capi.OK
+    assert geglu(T=0, gate=0, up=0, out=0) == _capi.OK
+    assert rms(C=0, x=0, res=0, w=0, out=0) == _capi.OK
+    assert tables(S=0, f=0, c=0, s=0) == _capi.OK
+
+
+def test_null_pointers(lib):
+    assert rope(x=0) == _capi.ERR_NULL
+    assert rope(cos=0) == _capi.ERR_NULL
+    assert rope(out=0) == _capi.ERR_NULL
+    assert geglu(up=0) == _capi.ERR_NULL
+    assert rms(w=0) == _capi.ERR_NULL
+    assert tables(s=0) == _capi.ERR_NULL
+
+
+def test_negative_and_overflowing_sizes(lib):
+    assert rope(S=-1) == _capi.ERR_SHAPE
+    assert rope(B=1 << 40, S=1 << 40) == _capi.ERR_SHAPE
+    assert geglu(F=-8) == _capi.ERR_SHAPE
+    assert geglu(T=1 << 62, F=1 << 2) == _capi.ERR_SHAPE
+    assert rms(T=-3) == _capi.ERR_SHAPE
+    assert tables(R=-2) == _capi.ERR_SHAPE
+
+
+def test_rot_dim(lib):
+    assert rope(rot=7) == _capi.ERR_ROTDIM
+    assert rope(rot=0) == _capi.ERR_ROTDIM
+    assert rope(rot=10) == _capi.ERR_ROTDIM  # > D
+    assert rope(rot=-2) == _capi.ERR_ROTDIM
+
+
+def test_strides(lib):
+    assert rope(sx_h=0) == _capi.ERR_STRIDE
+    assert rope(so_h=4) == _capi.ERR_STRIDE          # output heads overlap
+    assert rope(so_b=0, B=2) == _capi.ERR_STRIDE
+    assert geglu(sg=4) == _capi.ERR_STRIDE          # < F
+    assert geglu(so=7) == _capi.ERR_STRIDE
+    assert rms(sr=7) == _capi.ERR_STRIDE
+
+
+def test_aliasing(lib):
+    # out overlapping x but not identical
+    assert rope(out=P + 2) == _capi.ERR_ALIAS
+    # in place with different strides
+    assert rope(out=P, so_b=128, so_s=32, so_h=16, B=1) == _capi.ERR_ALIAS
+    # out overlapping the tables
+    assert rope(out=Q) == _capi.ERR_ALIAS
+    # GEGLU out over up
+    assert geglu(out=P + 16, so=16) == _capi.ERR_ALIAS
+    # out partially over gate
+    assert geglu(out=P + 8, so=16) == _capi.ERR_ALIAS
+    # RMSNorm: out over x / residual / w; x partly over residual; w inside residual rows
+    assert rms(out=P) == _capi.ERR_ALIAS
+    assert rms(out=Q) == _capi.ERR_ALIAS
+    assert rms(out=R) == _capi.ERR_ALIAS
+    assert rms(x=Q + 2) == _capi.ERR_ALIAS
+    assert rms(w=Q + 8) == _capi.ERR_ALIAS
+    # tables: cos and sin overlap
+    assert tables(s=Q + 2) == _capi.ERR_ALIAS
+    assert tables(c=P) == _capi.ERR_ALIAS
+
+
+def test_eps(lib):
+    assert rms(eps=-1.0) == _capi.ERR_VALUE
+    assert rms(eps=float("nan")) == _capi.ERR_VALUE
+    assert rms(eps=float("inf")) == _capi.ERR_VALUE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host without a GPU only")
+def test_valid_calls_report_missing_device(lib):
+    # arguments that pass validation reach the device check, which fails here
+    assert rope() == _capi.ERR_DEVICE
+    assert rope(out=P) == _capi.ERR_DEVICE          # in place is valid
+    assert geglu() == _capi.ERR_DEVICE              # gate/up halves of one buffer
+    assert geglu(out=P, so=16) == _capi.ERR_DEVICE  # out == gate in place
+    assert rms() == _capi.ERR_DEVICE
+    assert rms(x=Q, sx=8) == _capi.ERR_DEVICE       # x == residual
+    assert tables() == _capi.ERR_DEVICE
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = _capi._lib
+    _capi._lib = None
+    try:
+        with pytest.raises(_capi.DtrotUnavailable):
+            _capi.load(str(tmp_path / "missing.so"))
+    finally:
+        _capi._lib = saved

@@ -1,0 +1,357 @@
+"""GPU kernels (through the C ABI) against the CPU oracle, element by element.
+
+Bars: RoPE and the cos/sin tables bit-exact; GEGLU and RMSNorm within 1 bf16
+ulp everywhere with at most 0.01% of elements different (both are expected to
+be bit-exact by design; the mismatch count is printed).  Inputs are the seeded
+synthetic workloads; the full-size video layer runs in the launch
+configuration the benchmark times and is checked on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import diffusion_transformer_elementwise_rotate_b300 as dt
+from diffusion_transformer_elementwise_rotate_b300 import workloads as W
+from _compare import assert_bitexact, assert_within_tolerance, ulp_diff
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+EPS = float(np.float32(1e-6))
+bits = oracle.bf16_bits
+
+
+def to_dev(t):
+    return t.to(DEV, non_blocking=False)
+
+
+def from_u16(a):
+    return oracle.from_bits(a)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    dt.load()
+    torch.cuda.init()
+
+
+# ---------------------------------------------------------------- a1 tables
+
+@pytest.mark.parametrize("name", ["tiny", "image", "cfg", "video"])
+def test_cos_sin_tables_bitexact(name):
+    wl = W.WORKLOADS[name]
+    freqs = W.freqs_for(wl)
+    c, s = dt.rope_cos_sin_precompute(to_dev(freqs))
+    ec, es = oracle.rope_cos_sin(freqs.numpy())
+    assert_bitexact(bits(c), ec, f"{name} cos")
+    assert_bitexact(bits(s), es, f"{name} sin")
+
+
+@pytest.mark.parametrize("shape", [(3, 5, 1, 6), (7, 2, 1, 16), (1000, 1, 1, 8)])
+def test_cos_sin_random_and_special_angles(shape):
+    g = torch.Generator().manual_seed(17)
+    n = int(np.prod(shape))
+    f = torch.empty(n, dtype=torch.float32)
+    f.uniform_(-200.0, 200.0, generator=g)
+    special = torch.tensor([0.0, -0.0, 1e-30, -1e-40, 1.5707964, 3.1415927, 4.712389, 1e4,
+                            -3.3e4, 1e6, 1e30, float("inf"), float("-inf"), float("nan")])
+    k = min(n, special.numel())
+    f[:k] = special[:k]
+    f = f.view(*shape)
+    c, s = dt.rope_cos_sin_precompute(to_dev(f))
+    ec, es = oracle.rope_cos_sin(f.numpy())
+    assert_bitexact(bits(c), ec, "cos")
+    assert_bitexact(bits(s), es, "sin")
+
+
+def test_cos_sin_many_angles_near_rounding_midpoints():
+    # 4M angles spread over the position * frequency range of the workloads
+    g = torch.Generator().manual_seed(5)
+    f = (torch.rand(1 << 22, generator=g) * 60.0 - 5.0).view(-1, 1, 1, 64)
+    c, s = dt.rope_cos_sin_precompute(to_dev(f))
+    ec, es = oracle.rope_cos_sin(f.numpy())
+    assert_bitexact(bits(c), ec, "cos")
+    assert_bitexact(bits(s), es, "sin")
+
+
+# ---------------------------------------------------------------- a2 RoPE
+
+def _rope_case(x, cos_b, sin_b, **kw):
+    got = dt.rope_rotate_half(to_dev(x), to_dev(from_u16(cos_b)), to_dev(from_u16(sin_b)), **kw)
+    return bits(got)
+
+
+@pytest.mark.parametrize("name", ["tiny", "image", "cfg"])
+@pytest.mark.parametrize("which", ["q", "k"])
+def test_rope_configs_bitexact(name, which):
+    wl = W.WORKLOADS[name]
+    x = W.rope_inputs(wl, which)
+    cos_b, sin_b = oracle.rope_cos_sin(W.freqs_for(wl).numpy())
+    exp = oracle.rope_rotate_half(bits(x), cos_b, sin_b)
+    assert_bitexact(_rope_case(x, cos_b, sin_b), exp, f"{name} {which}")
+
+
+def test_rope_video_full_size_sampled_tokens():
+    wl = W.WORKLOADS["video"]
+    x = W.rope_inputs(wl, "q")
+    freqs = W.freqs_for(wl)
+    cd, sd = dt.rope_cos_sin_precompute(to_dev(freqs))
+    out = dt.rope_rotate_half(to_dev(x), cd, sd)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(wl.S, 1024, replace=False))
+    toks = np.concatenate([[0, wl.S - 1], toks])
+    cos_b, sin_b = bits(cd)[toks], bits(sd)[toks]
+    xs = bits(x)[:, toks]
+    exp = oracle.rope_rotate_half(xs, cos_b, sin_b)
+    assert_bitexact(bits(out)[:, toks], exp, "video sampled")
+
+
+SWEEP = [(64, 32), (64, 48), (64, 64), (80, 40), (80, 60), (80, 80), (128, 64), (128, 96),
+         (128, 128)]
+
+
+@pytest.mark.parametrize("D,rot", SWEEP)
+def test_rope_sweep_odd_S(D, rot):
+    B, S = 1, 4097
+    H = max(1, (1 << 20) // (S * D))
+    x = W.normal_bf16((B, S, H, D), 40 + D + rot, 0)
+    cos_b, sin_b = oracle.rope_cos_sin(W.freqs_1d(S, B, rot).numpy())
+    exp = oracle.rope_rotate_half(bits(x), cos_b, sin_b)
+    assert_bitexact(_rope_case(x, cos_b, sin_b), exp, f"D={D} rot={rot}")
+
+
+def test_rope_unrelated_table_halves_strided_qkv_and_misaligned():
+    rng = np.random.default_rng(3)
+    B, S, H, D, rot = 2, 37, 3, 128, 96
+    qkv = W.normal_bf16((B, S, 3 * H, D), 21, 0)
+    cos_b = oracle.rn16_array(rng.uniform(-2, 2, (B * S, rot)))
+    sin_b = oracle.rn16_array(rng.uniform(-2, 2, (B * S, rot)))
+    dq = to_dev(qkv)
+    k_view = dq[:, :, H:2 * H]                      # strided view, 16-byte aligned
+    got = dt.rope_rotate_half(k_view, to_dev(from_u16(cos_b)), to_dev(from_u16(sin_b)))
+    exp = oracle.rope_rotate_half(bits(qkv)[:, :, H:2 * H], cos_b, sin_b)
+    assert_bitexact(bits(got), exp, "strided k")
+    # one element off the 16-byte grid: the scalar path
+    flat = torch.empty(B * S * H * D + 1, dtype=torch.bfloat16, device=DEV)
+    xm = flat[1:].view(B, S, H, D)
+    xm.copy_(dq[:, :, :H])
+    om = torch.empty(B * S * H * D + 1, dtype=torch.bfloat16, device=DEV)[1:].view(B, S, H, D)
+    dt.rope_rotate_half(xm, to_dev(from_u16(cos_b)), to_dev(from_u16(sin_b)), out=om)
+    exp = oracle.rope_rotate_half(bits(qkv)[:, :, :H], cos_b, sin_b)
+    assert_bitexact(bits(om), exp, "misaligned")
+
+
+@pytest.mark.parametrize("D,rot", [(128, 96), (80, 60), (64, 64)])
+def test_rope_in_place(D, rot):
+    B, S, H = 1, 333, 5
+    x = W.normal_bf16((B, S, H, D), 7, 1)
+    cos_b, sin_b = oracle.rope_cos_sin(W.freqs_1d(S, B, rot).numpy())
+    xd = to_dev(x)
+    r = dt.rope_rotate_half(xd, to_dev(from_u16(cos_b)), to_dev(from_u16(sin_b)), out=xd)
+    assert r.data_ptr() == xd.data_ptr()
+    assert_bitexact(bits(xd), oracle.rope_rotate_half(bits(x), cos_b, sin_b), "in place")
+
+
+def test_rope_exhaustive_x_and_special_values():
+    allx = np.arange(1 << 16, dtype=np.uint16)
+    partner = np.roll(allx, 12345)
+    x = np.stack([allx, partner], axis=-1).reshape(1, -1, 1, 2)
+    S = x.shape[1]
+    cases = [(0x3F80, 0x0000), (0x3F35, 0x3F35), (0xBE9A, 0x3F74), (0x3C23, 0xBF7F),
+             (0x0001, 0x0081), (0x7F80, 0x3F00), (0x7FC0, 0x0000), (0x1F80, 0x2000)]
+    for c, s in cases:
+        cos_b = np.full((S, 2), c, np.uint16)
+        sin_b = np.full((S, 2), s, np.uint16)
+        got = _rope_case(from_u16(x), cos_b, sin_b)
+        assert_bitexact(got, oracle.rope_rotate_half(x, cos_b, sin_b), f"c={c:#x} s={s:#x}")
+
+
+def test_rope_empty():
+    x = torch.empty((1, 0, 4, 64), dtype=torch.bfloat16, device=DEV)
+    c = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    out = dt.rope_rotate_half(x, c, c)
+    assert out.shape == x.shape
+
+
+# ---------------------------------------------------------------- a3 GEGLU
+
+def test_geglu_every_bf16_gate_value_bitexact():
+    gate = np.arange(1 << 16, dtype=np.uint16).reshape(256, 256)
+    up = np.full_like(gate, 0x3F80)
+    got = dt.gelu_and_mul(to_dev(from_u16(gate)), to_dev(from_u16(up)))
+    assert_bitexact(bits(got), oracle.gelu_and_mul(gate, up), "gelu table")
+
+
+def test_geglu_every_gate_with_random_up():
+    gate = np.arange(1 << 16, dtype=np.uint16).reshape(128, 512)
+    up = bits(W.normal_bf16((128, 512), 9, 3, std=3.0))
+    up[0, :8] = [0x0001, 0x8001, 0x7F80, 0xFF80, 0x7FC0, 0x0000, 0x8000, 0x7F7F]
+    got = bits(dt.gelu_and_mul(to_dev(from_u16(gate)), to_dev(from_u16(up))))
+    exp = oracle.gelu_and_mul(gate, up)
+    n = assert_within_tolerance(got, exp, "gelu x random up")
+    print(f"gelu x random up: {n} mismatches")
+    assert_bitexact(got, exp, "gelu x random up (bit-exact by design)")
+
+
+def _geglu_check(gu, F, rows=None, what=""):
+    dgu = to_dev(gu)
+    out = dt.gelu_and_mul_fused(dgu)
+    torch.cuda.synchronize()
+    g = bits(gu)
+    if rows is None:
+        rows = np.arange(gu.shape[0])
+    exp = oracle.gelu_and_mul(g[rows, :F], g[rows, F:])
+    got = bits(out)[rows]
+    n = assert_within_tolerance(got, exp, what)
+    print(f"{what}: {n} mismatches of {got.size}")
+    assert_bitexact(got, exp, what)
+
+
+@pytest.mark.parametrize("name", ["tiny", "image", "cfg", "video"])
+def test_geglu_configs(name):
+    wl = W.WORKLOADS[name]
+    gu = W.geglu_inputs(wl)
+    rows = None
+    if wl.T_ff > 512:
+        rng = np.random.default_rng(1)
+        rows = np.unique(np.concatenate([[0, wl.T_ff - 1], rng.choice(wl.T_ff, 384, replace=False)]))
+    _geglu_check(gu, wl.F, rows, name)
+
+
+@pytest.mark.parametrize("F", [768, 2560, 4096, 5120, 12288, 13824, 1001])
+def test_geglu_sweep(F):
+    T = max(3, (1 << 20) // F) | 1
+    gu = W.normal_bf16((T, 2 * F), 60 + F, 2)
+    _geglu_check(gu, F, None, f"F={F}")
+
+
+def test_geglu_separate_buffers_misaligned_and_in_place():
+    T, F = 77, 520
+    g = W.normal_bf16((T, F + 3), 1, 2)
+    u = W.normal_bf16((T, F + 5), 1, 3)
+    gd, ud = to_dev(g), to_dev(u)
+    # distinct row strides, columns starting one element in (scalar path)
+    got = dt.gelu_and_mul(gd[:, 1:F + 1], ud[:, 2:F + 2])
+    exp = oracle.gelu_and_mul(bits(g)[:, 1:F + 1], bits(u)[:, 2:F + 2])
+    assert_bitexact(bits(got), exp, "misaligned")
+    # in place: out == gate
+    gate = to_dev(W.normal_bf16((T, F), 2, 2))
+    gate0 = bits(gate)
+    up = to_dev(W.normal_bf16((T, F), 2, 3))
+    r = dt.gelu_and_mul(gate, up, out=gate)
+    assert r.data_ptr() == gate.data_ptr()
+    assert_bitexact(bits(gate), oracle.gelu_and_mul(gate0, bits(up)), "in place")
+
+
+def test_geglu_empty():
+    z = torch.empty((0, 16), dtype=torch.bfloat16, device=DEV)
+    assert dt.gelu_and_mul(z, z).shape == (0, 16)
+
+
+# ---------------------------------------------------------------- a4 RMSNorm
+
+def _rms_check(x, r, w, rows=None, what="", exact=True):
+    xd, rd, wd = to_dev(x), to_dev(r), to_dev(w)
+    y = dt.rmsnorm_residual(xd, rd, wd, EPS)
+    torch.cuda.synchronize()
+    if rows is None:
+        rows = np.arange(x.shape[0])
+    h_exp, y_exp = oracle.rmsnorm_residual(bits(x)[rows], bits(r)[rows], bits(w), EPS)
+    assert_bitexact(bits(rd)[rows], h_exp, f"{what} residual")
+    got = bits(y)[rows]
+    n = assert_within_tolerance(got, y_exp, what)
+    print(f"{what}: {n} mismatches of {got.size}")
+    return n
+
+
+@pytest.mark.parametrize("name", ["tiny", "image", "cfg", "video"])
+@pytest.mark.parametrize("second", [False, True])
+def test_rmsnorm_configs(name, second):
+    wl = W.WORKLOADS[name]
+    x, r, w = W.rmsnorm_inputs(wl, second)
+    rows = None
+    if wl.T_norm > 512:
+        rng = np.random.default_rng(2)
+        rows = np.unique(np.concatenate([[0, wl.T_norm - 1],
+                                         rng.choice(wl.T_norm, 512, replace=False)]))
+    _rms_check(x, r, w, rows, name)
+
+
+@pytest.mark.parametrize("C", [768, 2560, 4096, 5120, 1, 7, 1001, 40000])
+def test_rmsnorm_sweep(C):
+    T = max(3, (1 << 20) // (C * 4)) | 1
+    x = W.normal_bf16((T, C), 80 + C, 4)
+    r = W.normal_bf16((T, C), 80 + C, 5, std=2.0)
+    w = W.normal_bf16((C,), 80 + C, 6, mean=1.0, std=0.316)
+    _rms_check(x, r, w, None, f"C={C}")
+
+
+def test_rmsnorm_special_rows():
+    C = 256
+    x = W.normal_bf16((8, C), 5, 4)
+    r = torch.zeros((8, C), dtype=torch.bfloat16)
+    x[1] = 0                      # all-zero row: y = 0
+    x[2] = 1e30                   # squares overflow fp32: double re-sum
+    x[3] *= 1e-30                 # squares underflow: double re-sum
+    x[4, 5] = float("nan")        # NaN row
+    x[5, 7] = float("inf")        # inf row
+    x[6] = 3.0                    # constant row
+    x[7] *= 2.0 ** -130           # subnormal inputs
+    w = W.normal_bf16((C,), 5, 6, mean=1.0, std=0.316)
+    _rms_check(x, r, w, None, "special rows")
+
+
+def test_rmsnorm_row_subsets_and_x_is_residual():
+    wl = W.WORKLOADS["tiny"]
+    x, r, w = W.rmsnorm_inputs(wl)
+    yd_full = dt.rmsnorm_residual(to_dev(x), to_dev(r.clone()), to_dev(w), EPS)
+    for a, b in [(0, 1), (3, 17), (100, 256)]:
+        ys = dt.rmsnorm_residual(to_dev(x[a:b]), to_dev(r[a:b].clone()), to_dev(w), EPS)
+        assert_bitexact(bits(ys), bits(yd_full)[a:b], f"rows {a}:{b}")
+    # x and residual the same buffer
+    xr = to_dev(r.clone())
+    y = dt.rmsnorm_residual(xr, xr, to_dev(w), EPS)
+    h_exp, y_exp = oracle.rmsnorm_residual(bits(r), bits(r), bits(w), EPS)
+    assert_bitexact(bits(xr), h_exp, "x is residual: h")
+    assert_within_tolerance(bits(y), y_exp, "x is residual: y")
+
+
+def test_rmsnorm_misaligned_generic_path():
+    T, C = 33, 512
+    x = W.normal_bf16((T, C + 1), 3, 4)
+    r = W.normal_bf16((T, C + 1), 3, 5, std=2.0)
+    w = W.normal_bf16((C + 1,), 3, 6, mean=1.0, std=0.316)
+    xd, rd, wd = to_dev(x), to_dev(r), to_dev(w)
+    y = dt.rmsnorm_residual(xd[:, 1:], rd[:, 1:], wd[1:], EPS)
+    h_exp, y_exp = oracle.rmsnorm_residual(bits(x)[:, 1:], bits(r)[:, 1:], bits(w)[1:], EPS)
+    assert_bitexact(bits(rd)[:, 1:], h_exp, "misaligned h")
+    assert_within_tolerance(bits(y), y_exp, "misaligned y")
+
+
+def test_rmsnorm_empty():
+    z = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones(64, dtype=torch.bfloat16, device=DEV)
+    assert dt.rmsnorm_residual(z, z.clone(), w).shape == (0, 64)
+
+
+# ---------------------------------------------------------------- misc
+
+def test_status_errors_raise():
+    x = torch.zeros((1, 4, 2, 8), dtype=torch.bfloat16, device=DEV)
+    c = torch.zeros((4, 6), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(dt.DtrotError):
+        dt.rope_rotate_half(x, c[:, :5].contiguous(), c[:, :5].contiguous())  # odd rot_dim
+
+
+def test_work_is_enqueued_on_the_current_stream():
+    wl = W.WORKLOADS["tiny"]
+    x = to_dev(W.rope_inputs(wl, "q"))
+    freqs = to_dev(W.freqs_for(wl))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c, sn = dt.rope_cos_sin_precompute(freqs)
+        out = dt.rope_rotate_half(x, c, sn)
+    s.synchronize()
+    cos_b, sin_b = oracle.rope_cos_sin(W.freqs_for(wl).numpy())
+    assert_bitexact(bits(out), oracle.rope_rotate_half(bits(x), cos_b, sin_b), "side stream")
