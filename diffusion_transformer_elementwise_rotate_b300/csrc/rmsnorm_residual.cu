@@ -10,20 +10,23 @@
 //
 // Design.  One CTA per token row; each thread holds VPT 8-column vectors of
 // the row in registers (one HBM read of x and residual, one write of h and
-// out; w is re-read from L1/L2).
+// out; w is re-read from L1/L2).  No fp64 on the common path: this part's
+// fp64 rate is a small fraction of its fp32 rate, so the row statistics are
+// carried in fp32 pairs ("double-float", value = hi + lo):
 //   - h = one add.rn.bf16x2 per packed pair (the bf16 rounding of x + r);
 //   - sum of h^2: each square is exact in fp32 (a bf16 has 8 significant
-//     bits), accumulated per thread with TwoSum compensation, combined across
-//     the warp as fp32 pairs with warp shuffles, and across warps in double by
-//     one thread, which also forms inv = (sum/C + eps)^(-1/2) in double;
-//   - out: h*w is exact in fp32; RN32(h*w*inv32) decides the bf16 rounding
-//     unless it lies within 3 fp32 ulps of a bf16 midpoint (or h*w left the
-//     fp32 normal range), where the value is recomputed as h*w*inv in double
-//     and rounded once.  So the output is the rounding of the fp64 result
-//     except in the rare rows where fp32-vs-fp64 summation order moves it
-//     across a midpoint.
-//   - rows whose fp32 sum of squares overflowed or is below 2^-60 (where
-//     squares may have underflowed) redo the sum in double.
+//     bits); TwoSum-compensated per thread, merged across the warp with
+//     shuffles and across warps through shared memory (every thread merges the
+//     warp partials in the same order, so all see the same total);
+//   - inv = (sum/C + eps)^(-1/2) as a double-float: rsqrtf seed plus one
+//     Newton step with an exactly computed residual (relative error ~2^-43);
+//   - out: h*w is exact in fp32; RN32(h*w*inv_hi) decides the bf16 rounding
+//     unless it lies within 2 fp32 ulps of a bf16 midpoint; there the product
+//     is formed as an exact fp32 pair (fma error term) and the midpoint is
+//     resolved by the sign of the low part.
+//   Only rows whose fp32 sum of squares overflowed or is tiny (< 2^-60, where
+//   squares may have underflowed) and elements outside the fp32 normal range
+//   (NaN, inf, |h*w| or |out| beyond 2^+-100) fall back to fp64.
 // A generic kernel (any alignment or width) loops over the row twice instead
 // of keeping it in registers.
 #include "dtrot_internal.cuh"
@@ -37,6 +40,12 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// |a| >= |b| (or a == 0)
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    e = __fsub_rn(b, __fsub_rn(s, a));
 }
 
 // acc (hi, lo) += v
@@ -53,19 +62,43 @@ __device__ __forceinline__ void acc_merge(float& hi, float& lo, float hi2, float
     lo = __fadd_rn(__fadd_rn(lo, lo2), e);
 }
 
+// Per-row statistics exchanged between warps; two slots alternate by row so a
+// warp starting the next row never overwrites values another warp still reads.
 struct RowShared {
-    float hi[kMaxWarps];
-    float lo[kMaxWarps];
+    float hi[2][kMaxWarps];
+    float lo[2][kMaxWarps];
     double dsum[kMaxWarps];
-    double inv_d;
-    float inv_f;
-    int redo;
 };
 
-// Block-wide reduction of the per-thread (hi, lo) pair; on return every
-// thread sees inv (double and fp32) and whether the row must redo its sum of
-// squares in double (then inv is not yet valid).
-__device__ __forceinline__ void block_sumsq(RowShared& sh, float hi, float lo) {
+// inv = (q + eps)^(-1/2) with q = (hi + lo) / C, as inv_hi + inv_lo.
+__device__ __forceinline__ void inv_rms_df(float hi, float lo, int64_t C, float eps,
+                                           float& inv_hi, float& inv_lo) {
+    const float Cf = (float)C;                       // exact for C < 2^24
+    const float q_hi = __fdiv_rn(hi, Cf);
+    const float rem = __fmaf_rn(-q_hi, Cf, hi);      // exact: hi - q_hi * C
+    const float q_lo = __fdiv_rn(__fadd_rn(rem, lo), Cf);
+    float s_hi, e;
+    two_sum(q_hi, eps, s_hi, e);
+    float s_lo = __fadd_rn(e, q_lo);
+    fast_two_sum(s_hi, s_lo, s_hi, s_lo);
+    const float y0 = rsqrtf(s_hi);
+    // residual 1 - s * y0^2, with y0^2 and s_hi * y0^2 formed exactly
+    const float p_hi = __fmul_rn(y0, y0);
+    const float p_lo = __fmaf_rn(y0, y0, -p_hi);
+    const float t_hi = __fmul_rn(s_hi, p_hi);
+    const float t_lo = __fmaf_rn(s_hi, p_hi, -t_hi);
+    float rr = __fsub_rn(1.0f, t_hi);                // exact: t_hi is close to 1
+    rr = __fsub_rn(rr, t_lo);
+    rr = __fsub_rn(rr, __fmaf_rn(s_hi, p_lo, __fmul_rn(s_lo, p_hi)));
+    const float corr = __fmul_rn(__fmul_rn(y0, rr), 0.5f);
+    fast_two_sum(y0, corr, inv_hi, inv_lo);
+}
+
+// Block-wide sum of squares.  Returns false when the row must redo the sum in
+// double (fp32 overflow, or a total small enough that squares may have
+// underflowed); the result is identical in every thread.
+__device__ __forceinline__ bool block_sumsq(RowShared& sh, int slot, float hi, float lo,
+                                            float& tot_hi, float& tot_lo) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -74,65 +107,77 @@ __device__ __forceinline__ void block_sumsq(RowShared& sh, float hi, float lo) {
         acc_merge(hi, lo, h2, l2);
     }
     if (lane == 0) {
-        sh.hi[warp] = hi;
-        sh.lo[warp] = lo;
+        sh.hi[slot][warp] = hi;
+        sh.lo[slot][warp] = lo;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0, fp32_mag = 0.0;
-        const int nw = (blockDim.x + 31) >> 5;
-        for (int w = 0; w < nw; ++w) {
-            t += (double)sh.hi[w] + (double)sh.lo[w];
-            fp32_mag += (double)sh.hi[w];
-        }
-        // an overflowed square makes hi inf (t inf or NaN); a tiny total may
-        // have lost underflowed squares
-        sh.redo = !(fabs(fp32_mag) < 1e38) || (t < 0x1p-60);
-        sh.dsum[0] = t;
-    }
-    __syncthreads();
+    const int nw = (blockDim.x + 31) >> 5;
+    float th = sh.hi[slot][0], tl = sh.lo[slot][0];
+    for (int w = 1; w < nw; ++w) acc_merge(th, tl, sh.hi[slot][w], sh.lo[slot][w]);
+    fast_two_sum(th, tl, tot_hi, tot_lo);
+    return (tot_hi <= 1e37f) && (tot_hi >= 0x1p-60f);  // false for NaN too
 }
 
-__device__ __forceinline__ void finish_inv(RowShared& sh, double total, int64_t C, float eps) {
-    const double inv = 1.0 / sqrt(total / (double)C + (double)eps);
-    sh.inv_d = inv;
-    sh.inv_f = __double2float_rn(inv);
-}
-
-// Block-wide double sum of per-thread partials (the redo path).
+// Block-wide double sum of per-thread partials (the rare redo path).
 __device__ __forceinline__ double block_sum_double(RowShared& sh, double v) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();  // everyone has read dsum[0] of the fp32 pass
     if (lane == 0) sh.dsum[warp] = v;
     __syncthreads();
+    const int nw = (blockDim.x + 31) >> 5;
     double t = 0.0;
-    if (threadIdx.x == 0) {
-        const int nw = (blockDim.x + 31) >> 5;
-        for (int w = 0; w < nw; ++w) t += sh.dsum[w];
-    }
+    for (int w = 0; w < nw; ++w) t += sh.dsum[w];
+    __syncthreads();  // dsum is reused by the next redo row
     return t;
 }
 
-// One output element from h and w (bf16 bits), with the midpoint check.
-__device__ __forceinline__ uint16_t norm_out(uint32_t hb, uint32_t wb, float inv_f,
-                                             double inv_d) {
-    const float h = __uint_as_float(hb << 16);
-    const float w = __uint_as_float(wb << 16);
-    const float hw = __fmul_rn(h, w);
-    const float y = __fmul_rn(hw, inv_f);
-    const float ahw = fabsf(hw);
-    const bool risky = (hw != 0.0f && !(ahw >= 0x1p-126f && ahw <= 0x1p127f)) ||
-                       !(fabsf(y) <= 0x1p127f) || ulps_to_bf16_midpoint(y) <= 3;
-    if (risky) return rn16d((double)h * (double)w * inv_d);  // NaN/inf follow IEEE here
-    return rn16f(y);
+__device__ __forceinline__ void inv_from_double(double total, int64_t C, float eps,
+                                                float& inv_hi, float& inv_lo) {
+    const double inv = 1.0 / sqrt(total / (double)C + (double)eps);
+    inv_hi = __double2float_rn(inv);
+    inv_lo = __double2float_rn(inv - (double)inv_hi);
 }
 
-__device__ __forceinline__ uint32_t norm_out2(uint32_t h2, uint32_t w2, float inv_f,
-                                              double inv_d) {
-    const uint32_t lo = norm_out(h2 & 0xFFFFu, w2 & 0xFFFFu, inv_f, inv_d);
-    const uint32_t hi = norm_out(h2 >> 16, w2 >> 16, inv_f, inv_d);
+// NaN, inf and extreme magnitudes: IEEE double (kept out of line so the
+// common path's register allocation does not carry it).
+__device__ __noinline__ uint16_t norm_out_rare(float h, float w, float inv_hi, float inv_lo) {
+    return rn16d((double)h * (double)w * ((double)inv_hi + (double)inv_lo));
+}
+
+// One output element from h and w (bf16 bits).
+__device__ __forceinline__ uint16_t norm_out(uint32_t hb, uint32_t wb, float inv_hi,
+                                             float inv_lo) {
+    const float h = __uint_as_float(hb << 16);
+    const float w = __uint_as_float(wb << 16);
+    const float hw = __fmul_rn(h, w);                 // exact in the normal range
+    const float y = __fmul_rn(hw, inv_hi);
+    const float ahw = fabsf(hw), ay = fabsf(y);
+    const bool normal = (ahw >= 0x1p-100f && ahw <= 0x1p100f && ay >= 0x1p-100f &&
+                         ay <= 0x1p100f);
+    if (normal) {
+        if (ulps_to_bf16_midpoint(y) > 2) return rn16f(y);
+        // exact pair for hw * inv_hi, plus hw * inv_lo
+        const float p_lo = __fmaf_rn(hw, inv_hi, -y);
+        const float y_lo = __fmaf_rn(hw, inv_lo, p_lo);
+        float y2, y2lo;
+        fast_two_sum(y, y_lo, y2, y2lo);
+        const uint32_t u = __float_as_uint(y2);
+        if ((u & 0xFFFFu) == 0x8000u && y2lo != 0.0f) {
+            // exactly on a midpoint in fp32: the low part decides
+            const bool away = (y2lo > 0.0f) == (y2 > 0.0f);
+            return (uint16_t)((u >> 16) + (away ? 1u : 0u));
+        }
+        return rn16f(y2);
+    }
+    if (hw == 0.0f && ay == 0.0f) return rn16f(y);    // exact zero (h or w is 0)
+    return norm_out_rare(h, w, inv_hi, inv_lo);
+}
+
+__device__ __forceinline__ uint32_t norm_out2(uint32_t h2, uint32_t w2, float inv_hi,
+                                              float inv_lo) {
+    const uint32_t lo = norm_out(h2 & 0xFFFFu, w2 & 0xFFFFu, inv_hi, inv_lo);
+    const uint32_t hi = norm_out(h2 >> 16, w2 >> 16, inv_hi, inv_lo);
     return lo | (hi << 16);
 }
 
@@ -147,15 +192,31 @@ __device__ __forceinline__ double sq_d2(uint32_t h2) {
     return a * a + b * b;
 }
 
+// Row statistics: inv = (mean(h^2) + eps)^(-1/2) as a double-float, from the
+// thread's compensated partial sum; `redo_sq` recomputes the thread's partial
+// in double when the fp32 total is out of range (uniform across the block).
+template <typename RedoSq>
+__device__ __forceinline__ void row_inv(RowShared& sh, int slot, float hi, float lo, int64_t C,
+                                        float eps, RedoSq redo_sq, float& inv_hi,
+                                        float& inv_lo) {
+    float th, tl;
+    if (block_sumsq(sh, slot, hi, lo, th, tl) && C < (1 << 24)) {
+        inv_rms_df(th, tl, C, eps, inv_hi, inv_lo);
+    } else {
+        const double t = block_sum_double(sh, redo_sq());
+        inv_from_double(t, C, eps, inv_hi, inv_lo);
+    }
+}
+
 // Vector path: C % 8 == 0, strides % 8 == 0, pointers 16-byte aligned,
-// C <= 8 * VPT * blockDim.
-// Threads per CTA are at most 256 for VPT <= 4 and 512 for VPT = 8, which
-// leaves 128 registers per thread for the row (x, residual and h vectors).
+// C <= 8 * VPT * blockDim.  Threads per CTA are at most 256 for VPT <= 4 and
+// 512 for VPT = 8, which leaves 128 registers per thread for the row.
 template <int VPT>
-__global__ void __launch_bounds__(VPT == 8 ? 512 : 256) rms_vec_kernel(RmsParams p) {
+__global__ void __launch_bounds__(VPT == 8 ? 512 : 256, VPT == 8 ? 1 : 4) rms_vec_kernel(RmsParams p) {
     __shared__ RowShared sh;
     const int64_t nv = p.C >> 3;
-    for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x) {
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, slot ^= 1) {
         const uint16_t* xr = p.x + row * p.sx;
         uint16_t* rr = p.residual + row * p.sr;
         uint16_t* orow = p.out + row * p.so;
@@ -185,36 +246,33 @@ __global__ void __launch_bounds__(VPT == 8 ? 512 : 256) rms_vec_kernel(RmsParams
                 sq_acc2(hv[k].w, hi, lo);
             }
         }
-        block_sumsq(sh, hi, lo);
-        if (sh.redo) {  // uniform across the block
-            double d = 0.0;
+        float inv_hi, inv_lo;
+        row_inv(sh, slot, hi, lo, p.C, p.eps,
+                [&]() {
+                    double d = 0.0;
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
-                if (v < nv) d += sq_d2(hv[k].x) + sq_d2(hv[k].y) + sq_d2(hv[k].z) + sq_d2(hv[k].w);
-            }
-            const double t = block_sum_double(sh, d);
-            if (threadIdx.x == 0) finish_inv(sh, t, p.C, p.eps);
-        } else if (threadIdx.x == 0) {
-            finish_inv(sh, sh.dsum[0], p.C, p.eps);
-        }
-        __syncthreads();
-        const float inv_f = sh.inv_f;
-        const double inv_d = sh.inv_d;
+                    for (int k = 0; k < VPT; ++k) {
+                        const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
+                        if (v < nv)
+                            d += sq_d2(hv[k].x) + sq_d2(hv[k].y) + sq_d2(hv[k].z) +
+                                 sq_d2(hv[k].w);
+                    }
+                    return d;
+                },
+                inv_hi, inv_lo);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
             if (v < nv) {
                 const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.w + v * 8));
                 uint4 o;
-                o.x = norm_out2(hv[k].x, wv.x, inv_f, inv_d);
-                o.y = norm_out2(hv[k].y, wv.y, inv_f, inv_d);
-                o.z = norm_out2(hv[k].z, wv.z, inv_f, inv_d);
-                o.w = norm_out2(hv[k].w, wv.w, inv_f, inv_d);
+                o.x = norm_out2(hv[k].x, wv.x, inv_hi, inv_lo);
+                o.y = norm_out2(hv[k].y, wv.y, inv_hi, inv_lo);
+                o.z = norm_out2(hv[k].z, wv.z, inv_hi, inv_lo);
+                o.w = norm_out2(hv[k].w, wv.w, inv_hi, inv_lo);
                 *reinterpret_cast<uint4*>(orow + v * 8) = o;
             }
         }
-        __syncthreads();  // sh is reused by the next row
     }
 }
 
@@ -222,7 +280,8 @@ __global__ void __launch_bounds__(VPT == 8 ? 512 : 256) rms_vec_kernel(RmsParams
 // accumulates; pass 2 re-reads the thread's own h values.
 __global__ void __launch_bounds__(256) rms_generic_kernel(RmsParams p) {
     __shared__ RowShared sh;
-    for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x) {
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, slot ^= 1) {
         const uint16_t* xr = p.x + row * p.sx;
         uint16_t* rr = p.residual + row * p.sr;
         uint16_t* orow = p.out + row * p.so;
@@ -233,25 +292,20 @@ __global__ void __launch_bounds__(256) rms_generic_kernel(RmsParams p) {
             const float hf = bf_lo(h);
             acc_add(hi, lo, __fmul_rn(hf, hf));
         }
-        block_sumsq(sh, hi, lo);
-        if (sh.redo) {
-            double d = 0.0;
-            for (int64_t c = threadIdx.x; c < p.C; c += blockDim.x) {
-                const double hf = (double)bf1(rr[c]);
-                d += hf * hf;
-            }
-            const double t = block_sum_double(sh, d);
-            if (threadIdx.x == 0) finish_inv(sh, t, p.C, p.eps);
-        } else if (threadIdx.x == 0) {
-            finish_inv(sh, sh.dsum[0], p.C, p.eps);
-        }
-        __syncthreads();
-        const float inv_f = sh.inv_f;
-        const double inv_d = sh.inv_d;
+        float inv_hi, inv_lo;
+        row_inv(sh, slot, hi, lo, p.C, p.eps,
+                [&]() {
+                    double d = 0.0;
+                    for (int64_t c = threadIdx.x; c < p.C; c += blockDim.x) {
+                        const double hf = (double)bf1(rr[c]);
+                        d += hf * hf;
+                    }
+                    return d;
+                },
+                inv_hi, inv_lo);
         for (int64_t c = threadIdx.x; c < p.C; c += blockDim.x) {
-            orow[c] = norm_out(rr[c], p.w[c], inv_f, inv_d);
+            orow[c] = norm_out(rr[c], p.w[c], inv_hi, inv_lo);
         }
-        __syncthreads();
     }
 }
 
