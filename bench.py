@@ -62,6 +62,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, pg, device=None) -> float:
+    """Max of a per-rank scalar (the timed region's duration) across ranks."""
+    if pg is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step: int, world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_step per step."""
+    return bytes_per_step * world * steps / (elapsed_ms / 1e3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -251,8 +265,9 @@ def cpu_baseline(wl, W, layer, target_s=15.0):
                    + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
         return dt_s, sampled, (tok, rows_ff, rows_n)
 
-    t, _, _ = run(1.0 / 2048)  # calibration
-    frac = min(1.0, (1.0 / 2048) * target_s / max(t, 1e-3))
+    run(1.0 / 2048)  # warm-up (thread pool start-up)
+    t, _, _ = run(1.0 / 256)  # calibration
+    frac = min(1.0, (1.0 / 256) * target_s / max(t, 1e-3))
     t, sampled, (tok, rf, rn) = run(frac)
     return {"value": round(sampled / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle",
@@ -308,12 +323,9 @@ def native(args):
     elapsed_ms = t_start.elapsed_time(t_end)
     kern_ms = {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
                for j, op in enumerate(OPS)}
-    if pg:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
     ms_per_step = elapsed_ms / K
-    value = per_step * world * K / (elapsed_ms / 1e3) / 1e9
+    value = aggregate_gbs(per_step, world, K, elapsed_ms)
 
     # end to end through host buffers: H2D inputs, the step, D2H outputs
     KE = max(1, args.e2e_steps)
@@ -333,11 +345,8 @@ def native(args):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = per_step * world * KE / (e2e_ms / 1e3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, pg, dev)
+    e2e_value = aggregate_gbs(per_step, world, KE, e2e_ms)
 
     if rank != 0:
         if pg:

@@ -160,6 +160,17 @@ def rmsnorm_inputs(wl: Workload, second: bool = False, pin: bool = False):
     return x, r, w
 
 
+def shard_rows(n: int, rank: int, world: int) -> tuple:
+    """Contiguous [lo, hi) slice of n token rows owned by `rank` of `world`
+    (sizes differ by at most one row).  Every op on this path is per token, so
+    shards need no exchange."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("rank must be in [0, world)")
+    base, extra = divmod(n, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
 def algorithmic_bytes(wl: Workload) -> dict:
     """Bytes each op must move at minimum (read inputs once, write outputs once)."""
     return {
