@@ -39,6 +39,8 @@ FALLBACK_HBM_GBS = 6400.0
 OPS = ["rope_cos_sin_precompute", "rope_rotate_half_q", "rope_rotate_half_k", "gelu_and_mul",
        "rmsnorm_residual_attn", "rmsnorm_residual_ffn"]
 DOMINANT = "gelu_and_mul"
+# kernels per step: tables 1, RoPE 2, GEGLU 2 (activation table + streaming), RMSNorm 2
+LAUNCHES_PER_STEP = 7
 
 
 def parse():
@@ -391,7 +393,7 @@ def native(args):
                      "algorithmic_bytes": bts[DOMINANT]},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": hb,
                 "d2h_bytes_per_step": db, "steps": KE},
-        "gpu_launches": 6 * K,
+        "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -6,5 +6,5 @@ RMSNorm fused with the residual add.  The torch wrappers in `api` only pass
 pointers, sizes and strides; `_capi` is the raw ctypes binding.
 """
 from ._capi import DtrotError, DtrotUnavailable, load  # noqa: F401
-from .api import (gelu_and_mul, gelu_and_mul_fused, rmsnorm_residual,  # noqa: F401
-                  rope_cos_sin_precompute, rope_rotate_half)
+from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_workspace,  # noqa: F401
+                  rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half)

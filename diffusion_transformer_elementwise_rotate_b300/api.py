@@ -7,16 +7,21 @@ runs in libdtrot's sm_103a kernels.
 
   rope_cos_sin_precompute(freqs)         -> (cos, sin)   ERNIE-Image page, section 1
   rope_rotate_half(x, cos, sin, out=None) -> out         ERNIE-Image page, section 2
-  gelu_and_mul(gate, up, out=None)        -> out         ERNIE-Image page, section 3
+  gelu_and_mul(gate, up, out=None, workspace=None) -> out     ERNIE-Image page, section 3
   gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
   rmsnorm_residual(x, residual, w, eps=1e-6, out=None) -> out   (residual updated in place)
                                                          sequence-parallelism post
 """
 from __future__ import annotations
 
+import threading
+
 import torch
 
 from . import _capi
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
 
 
 def _stream(t: torch.Tensor) -> int:
@@ -94,9 +99,24 @@ def _rows(t: torch.Tensor, name: str):
     return t.stride(0) if t.shape[0] > 1 else t.shape[1]
 
 
-def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor,
-                 out: torch.Tensor | None = None) -> torch.Tensor:
-    """gate, up bf16 (T, F) (row strides allowed) -> out bf16 (T, F)."""
+def gelu_workspace(device: torch.device, stream: int) -> torch.Tensor:
+    """The GEGLU workspace used for calls on (device, stream): one buffer per
+    stream, so calls that may overlap on the GPU never share one."""
+    key = (torch.device(device).index, int(stream))
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None:
+            n = int(_capi.load().dtrot_gelu_and_mul_workspace_bytes())
+            ws = torch.empty(n, dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+    return ws
+
+
+def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """gate, up bf16 (T, F) (row strides allowed) -> out bf16 (T, F).
+    `workspace` (a CUDA buffer of dtrot_gelu_and_mul_workspace_bytes() bytes)
+    defaults to a buffer cached per device and stream."""
     _need(gate, "gate", torch.bfloat16)
     _need(up, "up", torch.bfloat16)
     if gate.shape != up.shape:
@@ -109,8 +129,14 @@ def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor,
     if out.shape != gate.shape:
         raise ValueError("out must be (T, F)")
     so = _rows(out, "out")
+    st = _stream(gate)
+    if workspace is None:
+        workspace = gelu_workspace(gate.device, st)
+    elif not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
     _capi.check("dtrot_gelu_and_mul", gate.data_ptr(), sg, up.data_ptr(), su, out.data_ptr(),
-                so, T, F, _stream(gate))
+                so, T, F, workspace.data_ptr(), nbytes, st)
     return out
 
 

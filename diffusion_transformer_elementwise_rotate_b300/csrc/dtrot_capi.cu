@@ -120,6 +120,25 @@ bool row_disjoint(const uint16_t* w, int64_t cols, const uint16_t* v, int64_t sv
     return views2d_disjoint(v, sv, w, sv, rows, cols);
 }
 
+// A byte range [p, p + bytes) against a (rows, cols) bf16 view with row
+// stride sv: disjoint if the byte ranges are, or if the range lies wholly in
+// the gap after one row (element-aligned offsets only; otherwise reported as
+// overlapping).
+bool range_disjoint(const void* p, int64_t bytes, const uint16_t* v, int64_t sv, int64_t rows,
+                    int64_t cols) {
+    int64_t sz[2] = {rows, cols}, st[2] = {sv, 1};
+    Range rv;
+    if (!span(v, 2, sz, st, 2, &rv)) return false;
+    const Range rp{(uintptr_t)p, (uintptr_t)p + (uintptr_t)bytes};
+    if (!overlap(rp, rv)) return true;
+    if (rows == 1 || sv <= cols) return false;
+    const intptr_t dbytes = (intptr_t)((uintptr_t)p - (uintptr_t)v);
+    if (dbytes < 0 || dbytes % 2 || bytes % 2) return false;
+    const int64_t d = (int64_t)(dbytes / 2), len = bytes / 2;
+    const int64_t t0 = d / sv;
+    return d - t0 * sv >= cols && d + len <= (t0 + 1) * sv;
+}
+
 dtrot_status launch_status(cudaError_t e) {
     if (e == cudaSuccess) return DTROT_OK;
     return DTROT_ERR_LAUNCH;
@@ -156,11 +175,17 @@ DTROT_API const char* dtrot_status_str(dtrot_status s) {
         case DTROT_ERR_LAUNCH: return "DTROT_ERR_LAUNCH: the CUDA launch failed";
         case DTROT_ERR_DEVICE: return "DTROT_ERR_DEVICE: no sm_103 CUDA device is current";
         case DTROT_ERR_VALUE: return "DTROT_ERR_VALUE: a scalar argument is out of range";
+        case DTROT_ERR_WORKSPACE:
+            return "DTROT_ERR_WORKSPACE: the workspace is too small or not 16-byte aligned";
     }
     return "DTROT_ERR_UNKNOWN";
 }
 
-DTROT_API int dtrot_version(void) { return 100; }  // 0.1.0
+DTROT_API int dtrot_version(void) { return 200; }  // 0.2.0
+
+DTROT_API int64_t dtrot_gelu_and_mul_workspace_bytes(void) {
+    return (int64_t)gelu_table_bytes();
+}
 
 DTROT_API dtrot_status dtrot_rope_cos_sin_precompute(const float* freqs, int64_t S, int64_t B,
                                                      int64_t R, uint16_t* cos_out,
@@ -238,12 +263,15 @@ DTROT_API dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int6
 
 DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
                                           const uint16_t* up, int64_t s_up, uint16_t* out,
-                                          int64_t s_out, int64_t T, int64_t F, void* stream) {
+                                          int64_t s_out, int64_t T, int64_t F, void* workspace,
+                                          int64_t workspace_bytes, void* stream) {
     if (T < 0 || F < 0) return DTROT_ERR_SHAPE;
     int64_t n;
     if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
     if (n == 0) return DTROT_OK;
-    if (!gate || !up || !out) return DTROT_ERR_NULL;
+    if (!gate || !up || !out || !workspace) return DTROT_ERR_NULL;
+    if (workspace_bytes < (int64_t)gelu_table_bytes() || (uintptr_t)workspace % 16)
+        return DTROT_ERR_WORKSPACE;
     if (T > 1 && (s_gate < F || s_up < F || s_out < F)) return DTROT_ERR_STRIDE;
     if (s_gate < 0 || s_up < 0 || s_out < 0) return DTROT_ERR_STRIDE;
     const int64_t sg = T > 1 ? s_gate : F, su = T > 1 ? s_up : F, so = T > 1 ? s_out : F;
@@ -257,6 +285,14 @@ DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
     const bool in_place = (out == gate) && (so == sg);
     if (!in_place && !views2d_disjoint(out, so, gate, sg, T, F)) return DTROT_ERR_ALIAS;
     if (!views2d_disjoint(out, so, up, su, T, F)) return DTROT_ERR_ALIAS;
+    {
+        // the workspace is written: it must not overlap gate, up or out
+        const int64_t wb = (int64_t)gelu_table_bytes();
+        if (!range_disjoint(workspace, wb, gate, sg, T, F) ||
+            !range_disjoint(workspace, wb, up, su, T, F) ||
+            !range_disjoint(workspace, wb, out, so, T, F))
+            return DTROT_ERR_ALIAS;
+    }
     if (!device_ok()) return DTROT_ERR_DEVICE;
     GegluParams p;
     p.gate = gate;
@@ -267,7 +303,7 @@ DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
     p.s_out = so;
     p.T = T;
     p.F = F;
-    return launch_status(launch_gelu_and_mul(p, (cudaStream_t)stream));
+    return launch_status(launch_gelu_and_mul(p, (uint16_t*)workspace, (cudaStream_t)stream));
 }
 
 DTROT_API dtrot_status dtrot_rmsnorm_residual(const uint16_t* x, int64_t sx, uint16_t* residual,

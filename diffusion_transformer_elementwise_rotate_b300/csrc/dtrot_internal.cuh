@@ -117,7 +117,8 @@ int num_sms();  // SM count of the current device (cached)
 cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_t R,
                                 uint16_t* cos_out, uint16_t* sin_out, cudaStream_t st);
 cudaError_t launch_rope_rotate_half(const RopeParams& p, cudaStream_t st);
-cudaError_t launch_gelu_and_mul(const GegluParams& p, cudaStream_t st);
+size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
+cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);
 cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st);
 
 }  // namespace dtrot

@@ -6,12 +6,16 @@
 // does one, reproducing the bf16 rounding of the GELU output.
 //
 // Design.  gate is bf16, so the rounded activation g(gate) takes one of 65536
-// values.  Each CTA first tabulates g for every bf16 bit pattern in shared
-// memory (128 KB), then streams gate/up with 128-bit loads: per element one
-// shared-memory lookup and one bf16x2 multiply with .rn rounding.  The erf
-// arithmetic (tens of fp32 instructions per element, enough to make a direct
-// evaluation ALU-bound on this part) is paid 65536 times per CTA instead of
-// once per element, and the result is the exactly rounded GELU.
+// values.  A first kernel tabulates g for every bf16 bit pattern into a
+// 128 KB workspace, one entry per thread over the whole GPU.  The streaming
+// kernel is launched as its programmatic dependent: its persistent CTAs (one
+// per SM) start while the table kernel drains, wait for it in hardware
+// (griddepcontrol.wait), copy the table into shared memory and stream gate/up
+// with 128-bit loads: per element one shared-memory lookup and one bf16x2
+// multiply with .rn rounding.  The erf arithmetic (tens of fp32 instructions
+// per element, enough to make a direct evaluation ALU-bound on this part) is
+// paid 65536 times per call instead of once per element, and the result is
+// the exactly rounded GELU.
 //
 // Table entries: fp32 erfcf decides the rounding unless the fp32 value lies
 // within an error margin of a bf16 rounding midpoint (the margin grows with
@@ -62,8 +66,29 @@ __device__ __forceinline__ uint4 geglu_vec(const uint16_t* tab, uint4 g, uint4 u
     return o;
 }
 
-__device__ void build_table(uint16_t* tab) {
-    for (int i = threadIdx.x; i < kTable; i += blockDim.x) tab[i] = gelu_entry((uint32_t)i);
+__device__ __forceinline__ void grid_dependents_may_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Blocks until the grid this launch depends on (the table kernel) has
+// completed and its writes are visible; returns at once when the launch has
+// no programmatic dependency.
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// One table entry per thread: table[i] = RN16(RN32(gelu(bf16 bits i))).
+__global__ void __launch_bounds__(256) gelu_table_kernel(uint16_t* __restrict__ table) {
+    grid_dependents_may_launch();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < kTable) table[i] = gelu_entry((uint32_t)i);
+}
+
+// Copies the table from the workspace into shared memory (16 bytes per load).
+__device__ __forceinline__ void load_table(uint16_t* tab, const uint16_t* __restrict__ gtab) {
+    wait_for_prerequisite_grid();
+    const uint4* src = reinterpret_cast<const uint4*>(gtab);
+    uint4* dst = reinterpret_cast<uint4*>(tab);
+    for (int i = threadIdx.x; i < kTable / 8; i += blockDim.x) dst[i] = __ldcg(src + i);
     __syncthreads();
 }
 
@@ -71,9 +96,10 @@ __device__ void build_table(uint16_t* tab) {
 // Items are (row, 8-column vector) pairs, U per thread per iteration with all
 // loads of an iteration issued before its stores (safe for out == gate).
 template <int U>
-__global__ void __launch_bounds__(kThreads, 1) geglu_vec_kernel(GegluParams p) {
+__global__ void __launch_bounds__(kThreads, 1) geglu_vec_kernel(GegluParams p,
+                                                                const uint16_t* __restrict__ gtab) {
     extern __shared__ uint16_t tab[];
-    build_table(tab);
+    load_table(tab, gtab);
     const uint32_t nv = (uint32_t)(p.F >> 3);
     const int64_t items = p.T * (int64_t)nv;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -104,9 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1) geglu_vec_kernel(GegluParams p) {
 }
 
 // Scalar path for any alignment / width.
-__global__ void __launch_bounds__(kThreads, 1) geglu_scalar_kernel(GegluParams p) {
+__global__ void __launch_bounds__(kThreads, 1) geglu_scalar_kernel(GegluParams p,
+                                                                   const uint16_t* __restrict__ gtab) {
     extern __shared__ uint16_t tab[];
-    build_table(tab);
+    load_table(tab, gtab);
     const int64_t items = p.T * p.F;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -125,14 +152,16 @@ std::atomic<bool> g_attr[kMaxDev][2];  // dynamic shared memory attribute set, p
 
 }  // namespace
 
-cudaError_t launch_gelu_and_mul(const GegluParams& p, cudaStream_t st) {
+size_t gelu_table_bytes() { return kTable * sizeof(uint16_t); }
+
+cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st) {
     const size_t smem = kTable * sizeof(uint16_t);
     const bool vec = (p.F % 8 == 0) && (p.s_gate % 8 == 0) && (p.s_up % 8 == 0) &&
                      (p.s_out % 8 == 0) && aligned(p.gate, 16) && aligned(p.up, 16) &&
                      aligned(p.out, 16);
     const int sms = num_sms();
     // One CTA per SM (the table takes 128 KB of shared memory); fewer when the
-    // tensor is small, so tiny calls do not tabulate on every SM.
+    // tensor is small.
     const int64_t work = vec ? p.T * (p.F / 8) : p.T * p.F;
     int64_t blocks = (work + kThreads - 1) / kThreads;
     if (blocks > sms) blocks = sms;
@@ -150,10 +179,27 @@ cudaError_t launch_gelu_and_mul(const GegluParams& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         g_attr[dev][which].store(true, std::memory_order_release);
     }
+    gelu_table_kernel<<<kTable / 256, 256, 0, st>>>(table);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the streaming kernel may start before the table kernel completes; it
+    // waits for it with griddepcontrol.wait before touching the table
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint16_t* gtab = table;
     if (vec)
-        geglu_vec_kernel<4><<<(unsigned)blocks, kThreads, smem, st>>>(p);
+        e = cudaLaunchKernelEx(&cfg, geglu_vec_kernel<4>, p, gtab);
     else
-        geglu_scalar_kernel<<<(unsigned)blocks, kThreads, smem, st>>>(p);
+        e = cudaLaunchKernelEx(&cfg, geglu_scalar_kernel, p, gtab);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

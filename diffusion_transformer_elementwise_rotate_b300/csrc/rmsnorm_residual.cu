@@ -8,22 +8,25 @@
 // every other row.  The Pre-Norm layer figure adds the residual, then
 // normalises.
 //
-// Design.  One CTA per token row; each thread holds VPT 8-column vectors of
-// the row in registers (one HBM read of x and residual, one write of h and
-// out; w is re-read from L1/L2).  No fp64 on the common path: this part's
-// fp64 rate is a small fraction of its fp32 rate, so the row statistics are
-// carried in fp32 pairs ("double-float", value = hi + lo):
+// Design.  Persistent CTAs (as many as fit on the device), each working on one
+// token row at a time: thread t owns the 8-column vectors k * blockDim + t of
+// every row (VPT of them), keeps its w vectors in registers for the whole
+// launch, and loads the next row's x and residual vectors into registers while
+// it works on the current one.  One HBM read of x and residual, one write of h
+// and out per row.  No fp64 on the common path (this part's fp64 rate is a
+// small fraction of its fp32 rate), so the row statistics are carried in fp32
+// pairs ("double-float", value = hi + lo):
 //   - h = one add.rn.bf16x2 per packed pair (the bf16 rounding of x + r);
 //   - sum of h^2: each square is exact in fp32 (a bf16 has 8 significant
-//     bits); TwoSum-compensated per thread, merged across the warp with
-//     shuffles and across warps through shared memory (every thread merges the
-//     warp partials in the same order, so all see the same total);
+//     bits); accumulated with TwoSum on packed fp32x2 lanes, merged across the
+//     warp with shuffles and across warps through shared memory (every thread
+//     merges the warp partials in the same order, so all see the same total);
 //   - inv = (sum/C + eps)^(-1/2) as a double-float: rsqrtf seed plus one
 //     Newton step with an exactly computed residual (relative error ~2^-43);
 //   - out: h*w is exact in fp32; RN32(h*w*inv_hi) decides the bf16 rounding
-//     unless it lies within 2 fp32 ulps of a bf16 midpoint; there the product
-//     is formed as an exact fp32 pair (fma error term) and the midpoint is
-//     resolved by the sign of the low part.
+//     unless it lies within 2 fp32 ulps of a bf16 midpoint or outside
+//     [2^-90, 2^100]; there the product is formed as an exact fp32 pair (fma
+//     error term) and a midpoint is resolved by the sign of the low part.
 //   Only rows whose fp32 sum of squares overflowed or is tiny (< 2^-60, where
 //   squares may have underflowed) and elements outside the fp32 normal range
 //   (NaN, inf, |h*w| or |out| beyond 2^+-100) fall back to fp64.
@@ -208,70 +211,178 @@ __device__ __forceinline__ void row_inv(RowShared& sh, int slot, float hi, float
     }
 }
 
-// Vector path: C % 8 == 0, strides % 8 == 0, pointers 16-byte aligned,
-// C <= 8 * VPT * blockDim.  Threads per CTA are at most 256 for VPT <= 4 and
-// 512 for VPT = 8, which leaves 128 registers per thread for the row.
+// ---- packed fp32 pairs (two lanes per 64-bit register, one .rn rounding per lane)
+
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t add_x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub_x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16x2 word -> its two values as an exact fp32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// (hi, lo) += v lane-wise, TwoSum: hi + lo + v == new hi + new lo exactly up
+// to the rounding of the lo accumulation.
+__device__ __forceinline__ void acc_add_x2(uint64_t& hi, uint64_t& lo, uint64_t v) {
+    const uint64_t s = add_x2(hi, v);
+    const uint64_t bb = sub_x2(s, hi);
+    const uint64_t e = add_x2(sub_x2(hi, sub_x2(s, bb)), sub_x2(v, bb));
+    lo = add_x2(lo, e);
+    hi = s;
+}
+
+// Fast-path acceptance test for y = RN32(h * w * inv_hi): the bf16 rounding of
+// y is final when y is at least 3 fp32 ulps from a bf16 rounding midpoint and
+// 2^-90 <= |y| <= 2^100 (h * w exact, y normal).  NaN fails the range test.
+__device__ __forceinline__ bool y_settled(float y) {
+    const float a = fabsf(y);
+    const bool mid = ((__float_as_uint(y) + 0x8002u) & 0xFFFFu) <= 4u;
+    return (a >= 0x1p-90f) && (a <= 0x1p100f) && !mid;
+}
+
+// One token row on the vector path.  Thread t owns the 8-column vectors
+// v = k * blockDim + t (k < VPT, v < nv); xc, rc hold its x and residual
+// vectors of the row and wv its w vectors.
 template <int VPT>
-__global__ void __launch_bounds__(VPT == 8 ? 512 : 256, VPT == 8 ? 1 : 4) rms_vec_kernel(RmsParams p) {
+__device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int slot, int64_t row,
+                                        int nv, const uint4 (&xc)[VPT], const uint4 (&rc)[VPT],
+                                        const uint4 (&wv)[VPT]) {
+    const int tid = threadIdx.x;
+    // h = RN16(x + r), written back to the residual stream; exact squares
+    // accumulated lane-wise with TwoSum
+    uint4 hv[VPT];
+    uint64_t hi = 0, lo = 0;
+    uint4* rrow = reinterpret_cast<uint4*>(p.residual + row * p.sr);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * (int)blockDim.x + tid;
+        if (v < nv) {
+            hv[k].x = badd2(xc[k].x, rc[k].x);
+            hv[k].y = badd2(xc[k].y, rc[k].y);
+            hv[k].z = badd2(xc[k].z, rc[k].z);
+            hv[k].w = badd2(xc[k].w, rc[k].w);
+            rrow[v] = hv[k];
+            uint64_t f;
+            f = bf2_to_f2(hv[k].x);
+            acc_add_x2(hi, lo, mul_x2(f, f));
+            f = bf2_to_f2(hv[k].y);
+            acc_add_x2(hi, lo, mul_x2(f, f));
+            f = bf2_to_f2(hv[k].z);
+            acc_add_x2(hi, lo, mul_x2(f, f));
+            f = bf2_to_f2(hv[k].w);
+            acc_add_x2(hi, lo, mul_x2(f, f));
+        }
+    }
+    float shi = f2lo(hi), slo = f2lo(lo);
+    acc_merge(shi, slo, f2hi(hi), f2hi(lo));
+
+    float inv_hi, inv_lo;
+    row_inv(sh, slot, shi, slo, p.C, p.eps,
+            [&]() {
+                double d = 0.0;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * (int)blockDim.x + tid;
+                    if (v < nv)
+                        d += sq_d2(hv[k].x) + sq_d2(hv[k].y) + sq_d2(hv[k].z) + sq_d2(hv[k].w);
+                }
+                return d;
+            },
+            inv_hi, inv_lo);
+
+    // out = RN16(h * w * inv): RN32(RN32(h * w) * inv_hi) decides unless it is
+    // near a bf16 midpoint or outside the safe range (then the exact path).
+    // With inv <= 2^40, |y| >= 2^-90 implies |h * w| >= 2^-130, where the
+    // product of two bf16 values is exact in fp32; rows with a larger inverse
+    // (only possible through the double re-sum) take the exact path.
+    const bool fast_row = inv_hi <= 0x1p40f;
+    const uint64_t inv2 = f2(inv_hi, inv_hi);
+    uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.so);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * (int)blockDim.x + tid;
+        if (v < nv) {
+            const uint32_t hw[4] = {hv[k].x, hv[k].y, hv[k].z, hv[k].w};
+            const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t y = mul_x2(mul_x2(bf2_to_f2(hw[q]), bf2_to_f2(ww[q])), inv2);
+                const float y0 = f2lo(y), y1 = f2hi(y);
+                if (fast_row && y_settled(y0) && y_settled(y1))
+                    o[q] = rn16x2f(y0, y1);
+                else
+                    o[q] = norm_out2(hw[q], ww[q], inv_hi, inv_lo);
+            }
+            orow[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+template <int VPT>
+__device__ __forceinline__ void load_w(const RmsParams& p, int nv, uint4 (&wv)[VPT]) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * (int)blockDim.x + threadIdx.x;
+        if (v < nv) wv[k] = __ldg(reinterpret_cast<const uint4*>(p.w) + v);
+    }
+}
+
+// Vector path: C % 8 == 0, strides % 8 == 0, pointers 16-byte aligned,
+// C <= 8 * VPT * blockDim.  Persistent CTAs, one token row at a time;
+// each thread keeps its w vectors in registers for the whole launch and
+// prefetches the next row's x and residual vectors into registers while it
+// works on the current row.
+template <int VPT>
+__global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
     __shared__ RowShared sh;
-    const int64_t nv = p.C >> 3;
+    const int nv = (int)(p.C >> 3);
+    const int tid = threadIdx.x;
+    uint4 wv[VPT], xc[VPT], rc[VPT];
+    load_w<VPT>(p, nv, wv);
+    auto load_row = [&](int64_t r, uint4 (&xs)[VPT], uint4 (&rs)[VPT]) {
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + r * p.sx);
+        const uint4* rr = reinterpret_cast<const uint4*>(p.residual + r * p.sr);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * (int)blockDim.x + tid;
+            if (v < nv) {
+                xs[k] = xr[v];
+                rs[k] = rr[v];
+            }
+        }
+    };
+    int64_t row = blockIdx.x;
+    if (row < p.T) load_row(row, xc, rc);
     int slot = 0;
-    for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, slot ^= 1) {
-        const uint16_t* xr = p.x + row * p.sx;
-        uint16_t* rr = p.residual + row * p.sr;
-        uint16_t* orow = p.out + row * p.so;
-        uint4 hv[VPT];
-        uint4 xv[VPT], rv[VPT];
+    for (; row < p.T; row += gridDim.x, slot ^= 1) {
+        uint4 xn[VPT], rn[VPT];
+        const int64_t nrow = row + gridDim.x;
+        if (nrow < p.T) load_row(nrow, xn, rn);
+        rms_row<VPT>(p, sh, slot, row, nv, xc, rc, wv);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
-            if (v < nv) {
-                xv[k] = *reinterpret_cast<const uint4*>(xr + v * 8);
-                rv[k] = *reinterpret_cast<const uint4*>(rr + v * 8);
-            }
-        }
-        float hi = 0.0f, lo = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
-            if (v < nv) {
-                hv[k].x = badd2(xv[k].x, rv[k].x);
-                hv[k].y = badd2(xv[k].y, rv[k].y);
-                hv[k].z = badd2(xv[k].z, rv[k].z);
-                hv[k].w = badd2(xv[k].w, rv[k].w);
-                *reinterpret_cast<uint4*>(rr + v * 8) = hv[k];
-                sq_acc2(hv[k].x, hi, lo);
-                sq_acc2(hv[k].y, hi, lo);
-                sq_acc2(hv[k].z, hi, lo);
-                sq_acc2(hv[k].w, hi, lo);
-            }
-        }
-        float inv_hi, inv_lo;
-        row_inv(sh, slot, hi, lo, p.C, p.eps,
-                [&]() {
-                    double d = 0.0;
-#pragma unroll
-                    for (int k = 0; k < VPT; ++k) {
-                        const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
-                        if (v < nv)
-                            d += sq_d2(hv[k].x) + sq_d2(hv[k].y) + sq_d2(hv[k].z) +
-                                 sq_d2(hv[k].w);
-                    }
-                    return d;
-                },
-                inv_hi, inv_lo);
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int64_t v = (int64_t)k * blockDim.x + threadIdx.x;
-            if (v < nv) {
-                const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.w + v * 8));
-                uint4 o;
-                o.x = norm_out2(hv[k].x, wv.x, inv_hi, inv_lo);
-                o.y = norm_out2(hv[k].y, wv.y, inv_hi, inv_lo);
-                o.z = norm_out2(hv[k].z, wv.z, inv_hi, inv_lo);
-                o.w = norm_out2(hv[k].w, wv.w, inv_hi, inv_lo);
-                *reinterpret_cast<uint4*>(orow + v * 8) = o;
-            }
+            xc[k] = xn[k];
+            rc[k] = rn[k];
         }
     }
 }
@@ -311,10 +422,22 @@ __global__ void __launch_bounds__(256) rms_generic_kernel(RmsParams p) {
 
 bool aligned(const void* ptr, int bytes) { return ((uintptr_t)ptr % bytes) == 0; }
 
+// CTAs of `kernel` that fit on one SM at once (at least 1).
+template <typename K>
+cudaError_t per_sm_blocks(K kernel, int threads, size_t smem, int* n) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kernel, threads, smem);
+    if (*n < 1) *n = 1;
+    return e;
+}
+
 template <int VPT>
 cudaError_t launch_vec(const RmsParams& p, int threads, cudaStream_t st) {
-    int64_t blocks = p.T;
-    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    // persistent grid: as many CTAs as fit on the device at once, at most T
+    int per_sm = 0;
+    cudaError_t e = per_sm_blocks(rms_vec_kernel<VPT>, threads, 0, &per_sm);
+    if (e != cudaSuccess) return e;
+    int64_t blocks = (int64_t)num_sms() * per_sm;
+    if (blocks > p.T) blocks = p.T;
     rms_vec_kernel<VPT><<<(unsigned)blocks, threads, 0, st>>>(p);
     return cudaGetLastError();
 }
@@ -326,10 +449,12 @@ cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st) {
                      aligned(p.x, 16) && aligned(p.residual, 16) && aligned(p.w, 16) &&
                      aligned(p.out, 16);
     const int64_t nv = p.C / 8;
-    if (vec && nv <= 8 * 512) {
+    // VPT vectors per thread: the smallest of 1, 2, 4 that keeps a row within
+    // 160 threads, else 8 (up to 256 threads, C <= 16384)
+    if (vec && nv <= 8 * 256) {
         int vpt = 8;
-        for (int c : {1, 2, 4, 8}) {
-            if ((nv + c - 1) / c <= 256) {
+        for (int c : {1, 2, 4}) {
+            if ((nv + c - 1) / c <= 160) {
                 vpt = c;
                 break;
             }

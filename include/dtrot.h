@@ -55,7 +55,8 @@ typedef enum dtrot_status {
     DTROT_ERR_ALIAS = 5,  /* an output overlaps an input in a way the call does not allow */
     DTROT_ERR_LAUNCH = 6, /* the CUDA launch failed (see cudaGetLastError) */
     DTROT_ERR_DEVICE = 7, /* no current CUDA device, or it is not sm_103 */
-    DTROT_ERR_VALUE = 8   /* a scalar argument is out of range (eps) */
+    DTROT_ERR_VALUE = 8,  /* a scalar argument is out of range (eps) */
+    DTROT_ERR_WORKSPACE = 9 /* a workspace is smaller than required or not 16-byte aligned */
 } dtrot_status;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -108,6 +109,12 @@ dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int64_t S, int
                                     int64_t so_s, int64_t so_h, void* stream);
 
 /*
+ * Bytes of device workspace dtrot_gelu_and_mul needs (its activation table:
+ * 65536 bf16 entries, 131072 bytes).  Constant for a given library version.
+ */
+int64_t dtrot_gelu_and_mul_workspace_bytes(void);
+
+/*
  * GEGLU with the eager path's activation rounding.             [P4] section 3
  *
  *   out[t, f] = RN16(up[t, f] * RN16(RN32(gelu(gate[t, f]))))
@@ -120,10 +127,19 @@ dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int64_t S, int
  *   out       bf16, (T, F), row stride s_out >= F, written.  out == gate with
  *             s_out == s_gate (in place) is allowed; any other element overlap
  *             with gate or up is DTROT_ERR_ALIAS.
+ *   workspace device memory owned by the caller, at least
+ *             dtrot_gelu_and_mul_workspace_bytes() bytes (workspace_bytes says
+ *             how many), 16-byte aligned (else DTROT_ERR_WORKSPACE), not
+ *             overlapping gate, up or out (else DTROT_ERR_ALIAS).  Its contents
+ *             on entry are ignored; the call fills it with the activation table
+ *             (two kernels on `stream`: the table, then the streaming kernel as
+ *             its programmatic dependent).  Calls that may run at the same time
+ *             on the GPU must use different workspaces.
  */
 dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate, const uint16_t* up,
                                 int64_t s_up, uint16_t* out, int64_t s_out, int64_t T,
-                                int64_t F, void* stream);
+                                int64_t F, void* workspace, int64_t workspace_bytes,
+                                void* stream);
 
 /*
  * Token-wise RMSNorm fused with the residual add (Pre-Norm).   [P5]

@@ -34,7 +34,8 @@ def declared_functions():
 def test_header_declares_the_four_ops():
     names = declared_functions()
     for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half", "dtrot_gelu_and_mul",
-               "dtrot_rmsnorm_residual", "dtrot_status_str", "dtrot_version"):
+               "dtrot_gelu_and_mul_workspace_bytes", "dtrot_rmsnorm_residual",
+               "dtrot_status_str", "dtrot_version"):
         assert op in names
 
 
@@ -48,7 +49,7 @@ def test_status_strings(lib):
     for code, name in _capi.STATUS.items():
         s = lib.dtrot_status_str(code).decode()
         assert s.startswith(name)
-    assert lib.dtrot_version() >= 100
+    assert lib.dtrot_version() >= 200
 
 
 P = 0x100000  # fake, 256-byte aligned device addresses (never dereferenced)
@@ -66,11 +67,15 @@ def rope(**kw):
                       a["so_b"], a["so_s"], a["so_h"], None)
 
 
+WS = 0x2100000   # fake workspace
+WS_BYTES = 131072
+
+
 def geglu(**kw):
-    a = dict(gate=P, sg=16, up=P + 16, su=16, out=W, so=8, T=4, F=8)
+    a = dict(gate=P, sg=16, up=P + 16, su=16, out=W, so=8, T=4, F=8, ws=WS, wsb=WS_BYTES)
     a.update(kw)
     return _capi.call("dtrot_gelu_and_mul", a["gate"], a["sg"], a["up"], a["su"], a["out"],
-                      a["so"], a["T"], a["F"], None)
+                      a["so"], a["T"], a["F"], a["ws"], a["wsb"], None)
 
 
 def rms(**kw):
@@ -100,6 +105,7 @@ def test_null_pointers(lib):
     assert rope(cos=0) == _capi.ERR_NULL
     assert rope(out=0) == _capi.ERR_NULL
     assert geglu(up=0) == _capi.ERR_NULL
+    assert geglu(ws=0) == _capi.ERR_NULL
     assert rms(w=0) == _capi.ERR_NULL
     assert tables(s=0) == _capi.ERR_NULL
 
@@ -149,6 +155,21 @@ def test_aliasing(lib):
     # tables: cos and sin overlap
     assert tables(s=Q + 2) == _capi.ERR_ALIAS
     assert tables(c=P) == _capi.ERR_ALIAS
+
+
+def test_gelu_workspace(lib):
+    assert lib.dtrot_gelu_and_mul_workspace_bytes() == WS_BYTES
+    assert geglu(wsb=WS_BYTES - 1) == _capi.ERR_WORKSPACE
+    assert geglu(wsb=0) == _capi.ERR_WORKSPACE
+    assert geglu(ws=WS + 8) == _capi.ERR_WORKSPACE            # not 16-byte aligned
+    assert geglu(ws=P) == _capi.ERR_ALIAS                      # over gate
+    assert geglu(ws=W - 64) == _capi.ERR_ALIAS                 # runs into out
+    # inside the gap between two long rows of gate/up: allowed
+    sg = 2 * 65536 + 64
+    assert geglu(sg=sg, su=sg, up=P + 16, ws=P + 2 * 32) in (_capi.ERR_DEVICE, _capi.OK)
+    # starts in that gap but runs into row 1 of gate (element sg)
+    assert geglu(sg=sg, su=sg, up=P + 16, ws=P + 2 * (sg - 65536 + 8)) == _capi.ERR_ALIAS
+    assert geglu(sg=sg, su=sg, up=P + 16, ws=P + 2 * sg) == _capi.ERR_ALIAS
 
 
 def test_eps(lib):

@@ -244,6 +244,22 @@ def test_geglu_separate_buffers_misaligned_and_in_place():
     assert_bitexact(bits(gate), oracle.gelu_and_mul(gate0, bits(up)), "in place")
 
 
+def test_geglu_caller_workspace_is_rebuilt_every_call():
+    # a caller-owned workspace holding garbage: the call fills in the table itself
+    from diffusion_transformer_elementwise_rotate_b300 import _capi
+    n = int(_capi.load().dtrot_gelu_and_mul_workspace_bytes())
+    gate = np.arange(1 << 16, dtype=np.uint16).reshape(64, 1024)
+    up = bits(W.normal_bf16((64, 1024), 11, 3))
+    exp = oracle.gelu_and_mul(gate, up)
+    for fill in (0xFF, 0x00, 0x7F):
+        ws = torch.full((n + 64,), fill, dtype=torch.uint8, device=DEV)[16:16 + n]
+        got = dt.gelu_and_mul(to_dev(from_u16(gate)), to_dev(from_u16(up)), workspace=ws)
+        assert_bitexact(bits(got), exp, f"workspace filled with {fill:#x}")
+    small = torch.empty(n - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(dt.DtrotError):
+        dt.gelu_and_mul(to_dev(from_u16(gate)), to_dev(from_u16(up)), workspace=small)
+
+
 def test_geglu_empty():
     z = torch.empty((0, 16), dtype=torch.bfloat16, device=DEV)
     assert dt.gelu_and_mul(z, z).shape == (0, 16)
@@ -278,7 +294,7 @@ def test_rmsnorm_configs(name, second):
     _rms_check(x, r, w, rows, name)
 
 
-@pytest.mark.parametrize("C", [768, 2560, 4096, 5120, 1, 7, 1001, 40000])
+@pytest.mark.parametrize("C", [768, 2560, 4096, 5120, 8192, 12288, 1, 7, 1001, 40000])
 def test_rmsnorm_sweep(C):
     T = max(3, (1 << 20) // (C * 4)) | 1
     x = W.normal_bf16((T, C), 80 + C, 4)
