@@ -40,6 +40,7 @@ SIGNATURES = {
     "dtrot_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
     "dtrot_gelu_and_mul": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p, _i64,
                                           _p]),
+    "dtrot_gelu_and_mul_noalloc": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p]),
     "dtrot_rmsnorm_residual": (ctypes.c_int,
                                [_p, _i64, _p, _i64, _p, ctypes.c_float, _p, _i64, _i64, _i64,
                                 _p]),

@@ -306,6 +306,32 @@ DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
     return launch_status(launch_gelu_and_mul(p, (uint16_t*)workspace, (cudaStream_t)stream));
 }
 
+// GEGLU for callers that cannot allocate device memory: the same computation
+// as dtrot_gelu_and_mul, with the activation table kept in the library's own
+// static device array instead of a caller workspace.
+DTROT_API dtrot_status dtrot_gelu_and_mul_noalloc(const uint16_t* gate, int64_t s_gate,
+                                                  const uint16_t* up, int64_t s_up, uint16_t* out,
+                                                  int64_t s_out, int64_t T, int64_t F,
+                                                  void* stream) {
+    if (T < 0 || F < 0) return DTROT_ERR_SHAPE;
+    int64_t n;
+    if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!gate || !up || !out) return DTROT_ERR_NULL;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    uint16_t* table = nullptr;
+    size_t capacity = 0;
+    if (noalloc_gelu_table(&table, &capacity) != cudaSuccess) {
+        cudaGetLastError();
+        return DTROT_ERR_DEVICE;
+    }
+    // the table's size is fixed (it does not grow with T or F); a library
+    // whose table outgrew the static array would refuse every call here
+    if (gelu_table_bytes() > capacity) return DTROT_ERR_WORKSPACE;
+    return dtrot_gelu_and_mul(gate, s_gate, up, s_up, out, s_out, T, F, table,
+                              (int64_t)capacity, stream);
+}
+
 DTROT_API dtrot_status dtrot_rmsnorm_residual(const uint16_t* x, int64_t sx, uint16_t* residual,
                                               int64_t sr, const uint16_t* w, float eps,
                                               uint16_t* out, int64_t so, int64_t T, int64_t C,

@@ -119,6 +119,9 @@ cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_
 cudaError_t launch_rope_rotate_half(const RopeParams& p, cudaStream_t st);
 size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);
+// Device address and size of the library-owned activation table of the
+// current device (looked up on the first call per device).
+cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity);
 cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st);
 
 }  // namespace dtrot

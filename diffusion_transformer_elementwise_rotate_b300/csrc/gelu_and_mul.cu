@@ -150,9 +150,36 @@ bool aligned(const void* ptr, int bytes) { return ((uintptr_t)ptr % bytes) == 0;
 constexpr int kMaxDev = 64;
 std::atomic<bool> g_attr[kMaxDev][2];  // dynamic shared memory attribute set, per device
 
+// Activation table owned by the library, for callers that cannot hand in a
+// workspace (dtrot_gelu_and_mul_noalloc).  One copy per device that loads the
+// library, 128 KB, kept until the process exits.  Host code may not use this
+// name as a device address: it is a host-side stand-in, and its device address
+// comes from cudaGetSymbolAddress.
+static __device__ __align__(256) uint16_t g_noalloc_table[kTable];
+std::atomic<uintptr_t> g_noalloc_addr[kMaxDev];  // device address, once per device
+
 }  // namespace
 
 size_t gelu_table_bytes() { return kTable * sizeof(uint16_t); }
+
+cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    uintptr_t a = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (a == 0) {
+        // first use on this device (which is current): look up the address
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_table);
+        if (e != cudaSuccess) return e;
+        a = (uintptr_t)ptr;
+        g_noalloc_addr[dev].store(a, std::memory_order_release);
+    }
+    *table = reinterpret_cast<uint16_t*>(a);
+    *capacity = sizeof(g_noalloc_table);
+    return cudaSuccess;
+}
 
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st) {
     const size_t smem = kTable * sizeof(uint16_t);

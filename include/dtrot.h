@@ -142,6 +142,36 @@ dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate, const uint
                                 void* stream);
 
 /*
+ * GEGLU that allocates nothing and needs no workspace.  The paper has no
+ * counterpart to this entry point; it is an addition of this library.
+ *
+ * Same arguments, result and error codes as dtrot_gelu_and_mul, without the
+ * workspace.  For callers that cannot obtain device memory of their own: for
+ * example code embedded in a host framework that plans every device
+ * allocation ahead and hands the code only its input and output tensors (an
+ * extra cudaMalloc would break the framework's memory budget or is not
+ * permitted there), or a plain C caller that has no allocator to draw from.  The 128 KB activation table lives in a static device
+ * array inside this library instead; every GPU that loads the library holds
+ * one such array until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make that
+ *     first call before any stream capture on the device.
+ *   - The table's size does not depend on T or F, so no valid size is too big
+ *     for the array; if a library build's table ever exceeded the array, every
+ *     call would return DTROT_ERR_WORKSPACE.  T and F are limited as for
+ *     dtrot_gelu_and_mul (overflow: DTROT_ERR_SHAPE).
+ *   - All calls on a device share the one array and each call rewrites it in
+ *     full before reading it (nothing in it needs to start at zero).  Calls
+ *     that overlap on the GPU (different streams with no ordering between
+ *     them) race on it and may read a half-written table: order them, or use
+ *     dtrot_gelu_and_mul with one workspace per stream.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+dtrot_status dtrot_gelu_and_mul_noalloc(const uint16_t* gate, int64_t s_gate, const uint16_t* up,
+                                        int64_t s_up, uint16_t* out, int64_t s_out, int64_t T,
+                                        int64_t F, void* stream);
+
+/*
  * Token-wise RMSNorm fused with the residual add (Pre-Norm).   [P5]
  *
  * For every token row t:

@@ -1,0 +1,74 @@
+"""dtrot_gelu_and_mul_noalloc: GEGLU for callers that cannot allocate device
+memory (a framework that plans every allocation ahead and passes in only the
+input and output tensors, or a plain C caller with no allocator).  Its
+activation table lives in a static array inside the library rather than in a
+caller workspace.
+
+Called through the C ABI and checked against dtrot_gelu_and_mul (the entry
+point with a caller workspace) on two calls in a row, so the second call runs
+on the table the first one left in the shared array.  Runs alone in a fresh
+process as well as after the rest of the suite; the file name makes pytest
+collect it last.
+"""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_elementwise_rotate_b300 import _capi
+from diffusion_transformer_elementwise_rotate_b300 import build as dbuild
+from diffusion_transformer_elementwise_rotate_b300 import workloads as W
+from _compare import assert_within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dbuild.build()
+    torch.cuda.init()
+    return _capi.load()
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _geglu_both(lib, gate_up, F):
+    """(noalloc result, workspace result) for gate = columns [0, F), up = [F, 2F)."""
+    T = gate_up.shape[0]
+    st = torch.cuda.current_stream().cuda_stream
+    g, u = gate_up.data_ptr(), gate_up.data_ptr() + 2 * F
+    out_na = torch.empty((T, F), dtype=torch.bfloat16, device="cuda")
+    out_ws = torch.empty((T, F), dtype=torch.bfloat16, device="cuda")
+    n = int(lib.dtrot_gelu_and_mul_workspace_bytes())
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    rc = lib.dtrot_gelu_and_mul_noalloc(g, 2 * F, u, 2 * F, out_na.data_ptr(), F, T, F, st)
+    assert rc == _capi.OK, _capi.STATUS.get(rc, rc)
+    rc = lib.dtrot_gelu_and_mul(g, 2 * F, u, 2 * F, out_ws.data_ptr(), F, T, F, ws.data_ptr(), n,
+                                st)
+    assert rc == _capi.OK, _capi.STATUS.get(rc, rc)
+    torch.cuda.synchronize()
+    return _bits(out_na), _bits(out_ws)
+
+
+def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(lib):
+    # call 1: every bf16 gate value once, random up; call 2: an image-layer
+    # shaped block of seeded N(0, 1) gate/up
+    F1 = 1024
+    gate = np.arange(1 << 16, dtype=np.uint16).reshape(64, F1)
+    up = W.normal_bf16((64, F1), 21, 3).view(torch.int16).numpy().view(np.uint16)
+    gu1 = torch.from_numpy(np.concatenate([gate, up], axis=1).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    gu2 = W.normal_bf16((1024, 2 * 12288), 22, 2).cuda()
+    for gu, F, what in ((gu1, F1, "call 1"), (gu2, 12288, "call 2")):
+        got, exp = _geglu_both(lib, gu, F)
+        assert_within_tolerance(got, exp, what)
+        assert np.array_equal(got, exp), what   # the same kernels: identical bits
+
+
+def test_noalloc_rejects_invalid_sizes_without_launching(lib):
+    assert lib.dtrot_gelu_and_mul_noalloc(0, 8, 0, 8, 0, 8, 0, 8, None) == _capi.OK
+    assert lib.dtrot_gelu_and_mul_noalloc(16, 8, 32, 8, 48, 8, -1, 8, None) == _capi.ERR_SHAPE
+    assert lib.dtrot_gelu_and_mul_noalloc(16, 8, 32, 8, 48, 8, 1 << 62, 8, None) == \
+        _capi.ERR_SHAPE
+    assert lib.dtrot_gelu_and_mul_noalloc(0, 8, 32, 8, 48, 8, 4, 8, None) == _capi.ERR_NULL
