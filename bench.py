@@ -231,6 +231,39 @@ class Layer:
         return sum(self.h_out[k].numel() * self.h_out[k].element_size() for k in self.out_names)
 
 
+def fused_rope_qk(dt, layer, wl, reps):
+    """Device time of rope_rotate_half_qk_ (q and k rotated in place by one
+    launch) on copies of the layer's q and k: with the cos/sin tables, and with
+    the angles (cos/sin evaluated in the kernel, no table written or read).
+    Algorithmic bytes: the rotated columns of q and k read and written once,
+    plus the tables (2 x 2 bytes) or the angles (4 bytes) per token and column."""
+    d = layer.d
+    q2, k2 = d["q"].clone(), d["k"].clone()
+    tok, rot, rows = wl.B * wl.S, wl.rot, 2 * wl.H
+    moved = 4 * tok * rows * rot
+    res = {}
+    for mode, kw, extra in (("tables", {"cos": d["cos"], "sin": d["sin"]}, 4 * tok * rot),
+                            ("angles", {"freqs": d["freqs"]}, 4 * tok * rot)):
+        for _ in range(3):
+            dt.rope_rotate_half_qk_(q2, k2, **kw)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            dt.rope_rotate_half_qk_(q2, k2, **kw)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[f"rope_qk_inplace_{mode}"] = {"ms": round(ms, 5), "bytes": moved + extra,
+                                          "gbs": round((moved + extra) / (ms / 1e3) / 1e9, 1),
+                                          "launches": 1, "reps": reps}
+    del q2, k2
+    res["note"] = ("in place, one launch for q and k; 'angles' also replaces the "
+                   "rope_cos_sin_precompute launch of the step")
+    return res
+
+
 def cpu_baseline(wl, W, layer, target_s=15.0):
     """Time the oracle (as it stands, all host cores it uses) on a bounded
     sample of the same workload: the first `frac` of each op's rows."""
@@ -329,6 +362,10 @@ def native(args):
     ms_per_step = elapsed_ms / K
     value = aggregate_gbs(per_step, world, K, elapsed_ms)
 
+    # the next rows on the same layer: RoPE on q and k in one in-place launch,
+    # with the tables or with the angles evaluated inside the kernel
+    fused = fused_rope_qk(dt, layer, wl, min(K, 200))
+
     # end to end through host buffers: H2D inputs, the step, D2H outputs
     KE = max(1, args.e2e_steps)
     layer.h2d()
@@ -394,6 +431,7 @@ def native(args):
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": hb,
                 "d2h_bytes_per_step": db, "steps": KE},
         "gpu_launches": LAUNCHES_PER_STEP * K,
+        "next_rows": fused,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -7,4 +7,5 @@ pointers, sizes and strides; `_capi` is the raw ctypes binding.
 """
 from ._capi import DtrotError, DtrotUnavailable, load  # noqa: F401
 from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_workspace,  # noqa: F401
-                  rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half)
+                  rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half,
+                  rope_rotate_half_qk_)

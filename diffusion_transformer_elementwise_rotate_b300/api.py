@@ -7,6 +7,8 @@ runs in libdtrot's sm_103a kernels.
 
   rope_cos_sin_precompute(freqs)         -> (cos, sin)   ERNIE-Image page, section 1
   rope_rotate_half(x, cos, sin, out=None) -> out         ERNIE-Image page, section 2
+  rope_rotate_half_qk_(q, k, cos=None, sin=None, freqs=None)   q and k in place, one launch;
+                                         tables, or angles evaluated in the kernel
   gelu_and_mul(gate, up, out=None, workspace=None) -> out     ERNIE-Image page, section 3
   gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
   rmsnorm_residual(x, residual, w, eps=1e-6, out=None) -> out   (residual updated in place)
@@ -90,6 +92,47 @@ def rope_rotate_half(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
                 cos.data_ptr(), sin.data_ptr(), rot, out.data_ptr(), so[0], so[1], so[2],
                 _stream(x))
     return out
+
+
+def rope_rotate_half_qk_(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | None = None,
+                         sin: torch.Tensor | None = None,
+                         freqs: torch.Tensor | None = None) -> None:
+    """Rotates q (B, S, Hq, D) and k (B, S, Hk, D) in place with one launch.
+    Give either the cos/sin tables (bf16 (B*S, rot)) or the angles `freqs`
+    (fp32 (S, B, 1, rot)), from which the kernel evaluates the rows itself.
+    q and k may be the q and k head ranges of one fused QKV tensor."""
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be (B, S, H, D)")
+    if q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q and k must share B, S and D")
+    _last_contiguous(q, "q")
+    _last_contiguous(k, "k")
+    B, S, Hq, D = q.shape
+    Hk = k.shape[2]
+    if (freqs is None) == (cos is None and sin is None):
+        raise ValueError("give either cos and sin, or freqs")
+    if freqs is not None:
+        _need(freqs, "freqs", torch.float32)
+        if freqs.dim() != 4 or freqs.shape[:3] != (S, B, 1) or not freqs.is_contiguous():
+            raise ValueError("freqs must be contiguous (S, B, 1, rot)")
+        rot = freqs.shape[3]
+        cp = sp = 0
+        fp = freqs.data_ptr()
+    else:
+        _need(cos, "cos", torch.bfloat16)
+        _need(sin, "sin", torch.bfloat16)
+        if cos.dim() != 2 or cos.shape != sin.shape or cos.shape[0] != B * S:
+            raise ValueError("cos/sin must be (B*S, rot_dim)")
+        if not (cos.is_contiguous() and sin.is_contiguous()):
+            raise ValueError("cos/sin must be contiguous")
+        rot = cos.shape[1]
+        cp, sp, fp = cos.data_ptr(), sin.data_ptr(), 0
+    sq, sk = q.stride(), k.stride()
+    _capi.check("dtrot_rope_rotate_half_qk", q.data_ptr(), Hq, sq[0], sq[1], sq[2],
+                k.data_ptr(), Hk, sk[0], sk[1], sk[2], B, S, D, cp or None, sp or None,
+                fp or None, rot, _stream(q))
 
 
 def _rows(t: torch.Tensor, name: str):

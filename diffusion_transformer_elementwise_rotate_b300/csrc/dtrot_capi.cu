@@ -261,6 +261,86 @@ DTROT_API dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int6
     return launch_status(launch_rope_rotate_half(p, (cudaStream_t)stream));
 }
 
+DTROT_API dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_t sq_b,
+                                                 int64_t sq_s, int64_t sq_h, uint16_t* k,
+                                                 int64_t Hk, int64_t sk_b, int64_t sk_s,
+                                                 int64_t sk_h, int64_t B, int64_t S, int64_t D,
+                                                 const uint16_t* cos, const uint16_t* sin,
+                                                 const float* freqs, int64_t rot_dim,
+                                                 void* stream) {
+    if (B < 0 || S < 0 || Hq < 0 || Hk < 0 || D < 0) return DTROT_ERR_SHAPE;
+    int64_t ntok, rows, n;
+    if (!mul_ok(B, S, &ntok) || __builtin_add_overflow(Hq, Hk, &rows) ||
+        !mul_ok(ntok, rows, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 16, &n))
+        return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if ((Hq > 0 && !q) || (Hk > 0 && !k)) return DTROT_ERR_NULL;
+    if (freqs && (cos || sin)) return DTROT_ERR_VALUE;  // tables or angles, not both
+    if (!freqs && (!cos || !sin)) return DTROT_ERR_NULL;
+    if (rot_dim <= 0 || rot_dim % 2 || rot_dim > D) return DTROT_ERR_ROTDIM;
+    int64_t tab;
+    if (!mul_ok(ntok, rot_dim, &tab) || !mul_ok(tab, 4, &tab)) return DTROT_ERR_SHAPE;
+    tab /= 4;
+    const int64_t qsz[4] = {B, S, Hq, D}, ksz[4] = {B, S, Hk, D};
+    const int64_t qst[4] = {sq_b, sq_s, sq_h, 1}, kst[4] = {sk_b, sk_s, sk_h, 1};
+    for (int i = 0; i < 3; ++i) {
+        if (Hq > 0 && (qst[i] < 0 || (qsz[i] > 1 && qst[i] == 0))) return DTROT_ERR_STRIDE;
+        if (Hk > 0 && (kst[i] < 0 || (ksz[i] > 1 && kst[i] == 0))) return DTROT_ERR_STRIDE;
+    }
+    if ((Hq > 0 && !non_self_overlapping(qsz, qst, 4)) ||
+        (Hk > 0 && !non_self_overlapping(ksz, kst, 4)))
+        return DTROT_ERR_STRIDE;
+    Range rq{0, 0}, rk{0, 0};
+    if ((Hq > 0 && !span(q, 2, qsz, qst, 4, &rq)) || (Hk > 0 && !span(k, 2, ksz, kst, 4, &rk)))
+        return DTROT_ERR_SHAPE;
+    if (Hq > 0 && Hk > 0 && overlap(rq, rk)) {
+        // allowed when q and k are the two head ranges of one (B, S, Hq + Hk, D)
+        // view (the q and k parts of a fused QKV buffer), in either order
+        bool ok = sq_b == sk_b && sq_s == sk_s && sq_h == sk_h;
+        if (ok) {
+            const uint16_t* first = q < k ? q : k;
+            const uint16_t* second = q < k ? k : q;
+            const int64_t h_first = q < k ? Hq : Hk;
+            int64_t off;
+            ok = mul_ok(h_first, sq_h, &off) && second == first + off;
+            const int64_t usz[4] = {B, S, Hq + Hk, D};
+            ok = ok && non_self_overlapping(usz, qst, 4);
+        }
+        if (!ok) return DTROT_ERR_ALIAS;
+    }
+    // the read-only inputs must not overlap what is written
+    Range rin1, rin2{0, 0};
+    if (freqs) {
+        rin1 = Range{(uintptr_t)freqs, (uintptr_t)freqs + (uintptr_t)tab * 4};
+    } else {
+        rin1 = Range{(uintptr_t)cos, (uintptr_t)cos + (uintptr_t)tab * 2};
+        rin2 = Range{(uintptr_t)sin, (uintptr_t)sin + (uintptr_t)tab * 2};
+    }
+    for (const Range* r : {&rq, &rk})
+        if (r->hi > r->lo && (overlap(*r, rin1) || (rin2.hi > rin2.lo && overlap(*r, rin2))))
+            return DTROT_ERR_ALIAS;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    RopeQKParams p;
+    p.q = q;
+    p.k = k;
+    p.cos = freqs ? nullptr : cos;
+    p.sin = freqs ? nullptr : sin;
+    p.freqs = freqs;
+    p.B = B;
+    p.S = S;
+    p.Hq = Hq;
+    p.Hk = Hk;
+    p.D = D;
+    p.rot = rot_dim;
+    p.sq_b = sq_b;
+    p.sq_s = sq_s;
+    p.sq_h = sq_h;
+    p.sk_b = sk_b;
+    p.sk_s = sk_s;
+    p.sk_h = sk_h;
+    return launch_status(launch_rope_qk(p, (cudaStream_t)stream));
+}
+
 DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
                                           const uint16_t* up, int64_t s_up, uint16_t* out,
                                           int64_t s_out, int64_t T, int64_t F, void* workspace,

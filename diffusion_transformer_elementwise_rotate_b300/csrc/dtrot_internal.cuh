@@ -83,6 +83,30 @@ __device__ __forceinline__ uint16_t rn16d(double d) {
     return rn16f(fz);
 }
 
+// ------------------------------------------------------------ rotary tables
+
+// One table entry: c16 = RN16(RN32(cos f)), s16 = RN16(RN32(sin f)) with the
+// fp32 cos/sin taken as correctly rounded.  sincosf (fp32, within 2 ulps of
+// the exact value) decides the bf16 rounding unless its result lies within
+// kCosSinMargin fp32 ulps of a bf16 rounding midpoint; only then is the value
+// recomputed from the fp64 cos/sin (within 2 double ulps), rounded to fp32 and
+// then to bf16.  A few in 10^4 entries take that path, so the fp64 units stay
+// idle almost always.
+constexpr int kCosSinMargin = 4;
+
+__device__ __forceinline__ void cos_sin_entry(float f, uint16_t& c16, uint16_t& s16) {
+    float s32, c32;
+    sincosf(f, &s32, &c32);
+    if (ulps_to_bf16_midpoint(c32) <= kCosSinMargin) {
+        c32 = __double2float_rn(cos((double)f));
+    }
+    if (ulps_to_bf16_midpoint(s32) <= kCosSinMargin) {
+        s32 = __double2float_rn(sin((double)f));
+    }
+    c16 = rn16f(c32);
+    s16 = rn16f(s32);
+}
+
 // ------------------------------------------------------------ launchers
 
 struct RopeParams {
@@ -94,6 +118,17 @@ struct RopeParams {
     int64_t sx_b, sx_s, sx_h;
     int64_t so_b, so_s, so_h;
     int in_place;
+};
+
+struct RopeQKParams {
+    uint16_t* q;             // (B, S, Hq, D), strides sq_*, rotated in place
+    uint16_t* k;             // (B, S, Hk, D), strides sk_*, rotated in place
+    const uint16_t* cos;     // (B*S, rot) tables, or NULL when freqs is given
+    const uint16_t* sin;
+    const float* freqs;      // (S, B, 1, rot) angles, or NULL when tables are given
+    int64_t B, S, Hq, Hk, D, rot;
+    int64_t sq_b, sq_s, sq_h;
+    int64_t sk_b, sk_s, sk_h;
 };
 
 struct GegluParams {
@@ -117,6 +152,7 @@ int num_sms();  // SM count of the current device (cached)
 cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_t R,
                                 uint16_t* cos_out, uint16_t* sin_out, cudaStream_t st);
 cudaError_t launch_rope_rotate_half(const RopeParams& p, cudaStream_t st);
+cudaError_t launch_rope_qk(const RopeQKParams& p, cudaStream_t st);
 size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);
 // Device address and size of the library-owned activation table of the

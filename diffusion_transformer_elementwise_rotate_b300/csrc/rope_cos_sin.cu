@@ -5,11 +5,9 @@
 // laid out as (B*S, R) rows, row b*S + s.  The entry is defined as
 // RN16(RN32(cos f)) with the fp32 cos correctly rounded.
 //
-// Evaluation: sincosf (fp32, within 2 ulps of the exact value) decides the
-// bf16 rounding unless its result lies within a few fp32 ulps of a bf16
-// rounding midpoint; only then is the entry recomputed from the fp64 cos/sin
-// (within 2 double ulps), rounded to fp32 and then to bf16.  A few in 10^4
-// entries take that path, so the fp64 units stay idle almost always.
+// Evaluation (cos_sin_entry, shared with the fused q/k kernel): sincosf
+// decides the bf16 rounding unless its result lies near a bf16 rounding
+// midpoint, where the entry is recomputed in fp64.
 //
 // Layout: one thread per group of VEC consecutive columns of an output row;
 // the permute is index arithmetic on the read side.  The table is a few tens
@@ -19,21 +17,6 @@
 
 namespace dtrot {
 namespace {
-
-constexpr int kMargin = 4;  // fp32 ulps of slack around a bf16 midpoint
-
-__device__ __forceinline__ void cos_sin_entry(float f, uint16_t& c16, uint16_t& s16) {
-    float s32, c32;
-    sincosf(f, &s32, &c32);
-    if (ulps_to_bf16_midpoint(c32) <= kMargin) {
-        c32 = __double2float_rn(cos((double)f));
-    }
-    if (ulps_to_bf16_midpoint(s32) <= kMargin) {
-        s32 = __double2float_rn(sin((double)f));
-    }
-    c16 = rn16f(c32);
-    s16 = rn16f(s32);
-}
 
 // VEC = 8: R % 8 == 0 and every base pointer 16-byte aligned (freqs 32-byte).
 template <int VEC>

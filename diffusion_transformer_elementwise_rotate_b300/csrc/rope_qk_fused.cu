@@ -1,0 +1,261 @@
+// Rotate-half RoPE on q and k of one attention layer in a single launch, in
+// place, with the cos/sin rows either read from the (B*S, rot_dim) tables or
+// computed on the fly from the rotary angles.
+//
+// ERNIE-Image fusion page (sglang PR #34306 analysis): section 2 gives the
+// per-op bf16 rounding of the rotation, round(round(x1*cos1) + round(-x2*sin1)),
+// applied to q and to k of every layer; section 1 hoists the cos/sin
+// computation out of the per-projection path.  This kernel goes one step
+// further on both counts: q and k (for example the q and k head ranges of one
+// fused QKV buffer) are rotated by one launch, so a token's cos/sin row is
+// fetched once for both; and with angles given instead of tables the row is
+// evaluated per token inside the kernel (cos_sin_entry, the same evaluation as
+// the table kernel, hence the same bits) and never written to HBM.
+//
+// Fast path (hh = rot_dim / 2 and every stride and pointer a multiple of the
+// vector width VW, hh / VW <= 32, and rot_dim <= kMaxRot with angles):
+//   - one warp per token (b, s); lanes own NP = hh / VW pair items (columns
+//     j..j+VW and j+hh..j+hh+VW) and walk the q rows and then the k rows,
+//     RPW = 32 / NP rows per pass, U rows per batch with all loads of a batch
+//     issued before any of its stores; the first batch is loaded before the
+//     token's cos/sin row is fetched or evaluated;
+//   - with angles, the warp first evaluates the token's rot_dim (cos, sin)
+//     pairs, one column per lane at a time, into its slot of shared memory and
+//     then reads its vectors from there; the same registers serve every q and
+//     k head of the token;
+//   - tail columns [rot_dim, D) are not touched: in place they already hold x.
+// Generic path: one thread per (token, head row of q or k, pair index).
+#include "dtrot_internal.cuh"
+
+namespace dtrot {
+namespace {
+
+constexpr int kMaxRot = 256;  // angle-mode fast path: rot_dim <= kMaxRot
+constexpr int kWarps = 8;     // warps per CTA of the fast kernel
+
+template <int VW>
+struct QKVec;
+template <>
+struct QKVec<8> { using T = uint4; };
+template <>
+struct QKVec<4> { using T = uint2; };
+template <>
+struct QKVec<2> { using T = uint32_t; };
+
+template <int VW>
+__device__ __forceinline__ typename QKVec<VW>::T qk_ld(const uint16_t* p) {
+    return *reinterpret_cast<const typename QKVec<VW>::T*>(p);
+}
+template <int VW>
+__device__ __forceinline__ void qk_st(uint16_t* p, typename QKVec<VW>::T v) {
+    *reinterpret_cast<typename QKVec<VW>::T*>(p) = v;
+}
+
+// o1 = R(R(x1 c1) + R(-x2 s1)), o2 = R(R(x2 c2) + R(x1 s2)) on packed words
+__device__ __forceinline__ void qk_rot_word(uint32_t x1, uint32_t x2, uint32_t c1, uint32_t s1,
+                                            uint32_t c2, uint32_t s2, uint32_t& o1,
+                                            uint32_t& o2) {
+    o1 = bsub2(bmul2(x1, c1), bmul2(x2, s1));
+    o2 = badd2(bmul2(x2, c2), bmul2(x1, s2));
+}
+__device__ __forceinline__ void qk_rot(uint4 a, uint4 b, uint4 c1, uint4 s1, uint4 c2, uint4 s2,
+                                       uint4& o1, uint4& o2) {
+    qk_rot_word(a.x, b.x, c1.x, s1.x, c2.x, s2.x, o1.x, o2.x);
+    qk_rot_word(a.y, b.y, c1.y, s1.y, c2.y, s2.y, o1.y, o2.y);
+    qk_rot_word(a.z, b.z, c1.z, s1.z, c2.z, s2.z, o1.z, o2.z);
+    qk_rot_word(a.w, b.w, c1.w, s1.w, c2.w, s2.w, o1.w, o2.w);
+}
+__device__ __forceinline__ void qk_rot(uint2 a, uint2 b, uint2 c1, uint2 s1, uint2 c2, uint2 s2,
+                                       uint2& o1, uint2& o2) {
+    qk_rot_word(a.x, b.x, c1.x, s1.x, c2.x, s2.x, o1.x, o2.x);
+    qk_rot_word(a.y, b.y, c1.y, s1.y, c2.y, s2.y, o1.y, o2.y);
+}
+__device__ __forceinline__ void qk_rot(uint32_t a, uint32_t b, uint32_t c1, uint32_t s1,
+                                       uint32_t c2, uint32_t s2, uint32_t& o1, uint32_t& o2) {
+    qk_rot_word(a, b, c1, s1, c2, s2, o1, o2);
+}
+
+struct QKArgs {
+    RopeQKParams p;
+    int NP;   // pair items per head row
+    int RPW;  // head rows per warp pass
+};
+
+template <int VW, int U, bool ANGLES>
+__global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
+    using V = typename QKVec<VW>::T;
+    __shared__ __align__(16) uint16_t cs[kWarps][2][kMaxRot];  // angle mode: cos, sin row
+    const RopeQKParams& p = a.p;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int ri = lane / a.NP;
+    const int it = lane - ri * a.NP;
+    const bool active = ri < a.RPW;  // 32 may not be a multiple of NP
+    const int64_t ntok = p.B * p.S;
+    const int64_t warps = (int64_t)gridDim.x * kWarps;
+    const int64_t hh = p.rot >> 1;
+    const int64_t j = (int64_t)it * VW;
+    const int64_t rows = p.Hq + p.Hk;  // q rows, then k rows
+    const int64_t step = (int64_t)U * a.RPW;
+    for (int64_t tok = (int64_t)blockIdx.x * kWarps + w; tok < ntok; tok += warps) {
+        const int64_t b = tok / p.S;
+        const int64_t s = tok - b * p.S;
+        uint16_t* qb = p.q + b * p.sq_b + s * p.sq_s + j;
+        uint16_t* kb = p.k + b * p.sk_b + s * p.sk_s + j;
+        auto row_ptr = [&](int64_t r) {
+            return r < p.Hq ? qb + r * p.sq_h : kb + (r - p.Hq) * p.sk_h;
+        };
+        // the first batch of head rows is loaded before the cos/sin row is
+        // fetched or evaluated, so its memory latency overlaps that work
+        V xa[U], xb[U];
+        auto load_batch = [&](int64_t r0) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t r = r0 + (int64_t)u * a.RPW;
+                if (active && r < rows) {
+                    const uint16_t* ptr = row_ptr(r);
+                    xa[u] = qk_ld<VW>(ptr);
+                    xb[u] = qk_ld<VW>(ptr + hh);
+                }
+            }
+        };
+        load_batch(ri);
+        V c1, c2, s1, s2;
+        if constexpr (ANGLES) {
+            const float* fr = p.freqs + (s * p.B + b) * p.rot;
+            for (int64_t c = lane; c < p.rot; c += 32) {
+                uint16_t cv, sv;
+                cos_sin_entry(__ldg(fr + c), cv, sv);
+                cs[w][0][c] = cv;
+                cs[w][1][c] = sv;
+            }
+            __syncwarp();
+            if (active) {
+                c1 = qk_ld<VW>(&cs[w][0][j]);
+                c2 = qk_ld<VW>(&cs[w][0][j + hh]);
+                s1 = qk_ld<VW>(&cs[w][1][j]);
+                s2 = qk_ld<VW>(&cs[w][1][j + hh]);
+            }
+            __syncwarp();  // every lane has its row before the next token overwrites it
+        } else {
+            if (active) {
+                const uint16_t* ct = p.cos + tok * p.rot + j;
+                const uint16_t* st = p.sin + tok * p.rot + j;
+                c1 = qk_ld<VW>(ct);
+                c2 = qk_ld<VW>(ct + hh);
+                s1 = qk_ld<VW>(st);
+                s2 = qk_ld<VW>(st + hh);
+            }
+        }
+        if (!active) continue;
+        for (int64_t r0 = ri;;) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t r = r0 + (int64_t)u * a.RPW;
+                if (r < rows) {
+                    V o1, o2;
+                    qk_rot(xa[u], xb[u], c1, s1, c2, s2, o1, o2);
+                    uint16_t* ptr = row_ptr(r);
+                    qk_st<VW>(ptr, o1);
+                    qk_st<VW>(ptr + hh, o2);
+                }
+            }
+            r0 += step;
+            if (r0 >= rows) break;
+            load_batch(r0);
+        }
+    }
+}
+
+// Generic path: one thread per (token, head row, pair index i < hh); head rows
+// [0, Hq) are q's, [Hq, Hq + Hk) k's.
+template <bool ANGLES>
+__global__ void __launch_bounds__(256) rope_qk_generic_kernel(RopeQKParams p) {
+    const int64_t hh = p.rot >> 1;
+    const int64_t rows = p.Hq + p.Hk;
+    const int64_t per_tok = rows * hh;
+    const int64_t total = p.B * p.S * per_tok;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tok = g / per_tok;
+        const int64_t rem = g - tok * per_tok;
+        const int64_t r = rem / hh;
+        const int64_t i = rem - r * hh;
+        const int64_t b = tok / p.S;
+        const int64_t s = tok - b * p.S;
+        uint16_t* row = r < p.Hq ? p.q + b * p.sq_b + s * p.sq_s + r * p.sq_h
+                                 : p.k + b * p.sk_b + s * p.sk_s + (r - p.Hq) * p.sk_h;
+        uint32_t c1, c2, s1, s2;
+        if constexpr (ANGLES) {
+            const float* fr = p.freqs + (s * p.B + b) * p.rot;
+            uint16_t a0, b0, a1, b1;
+            cos_sin_entry(__ldg(fr + i), a0, b0);
+            cos_sin_entry(__ldg(fr + i + hh), a1, b1);
+            c1 = a0, s1 = b0, c2 = a1, s2 = b1;
+        } else {
+            c1 = p.cos[tok * p.rot + i];
+            c2 = p.cos[tok * p.rot + i + hh];
+            s1 = p.sin[tok * p.rot + i];
+            s2 = p.sin[tok * p.rot + i + hh];
+        }
+        uint32_t o1, o2;
+        qk_rot_word(row[i], row[i + hh], c1, s1, c2, s2, o1, o2);
+        row[i] = (uint16_t)o1;
+        row[i + hh] = (uint16_t)o2;
+    }
+}
+
+bool aligned(const void* ptr, int bytes) { return ((uintptr_t)ptr % bytes) == 0; }
+
+int pick_qk_vw(const RopeQKParams& p) {
+    const int64_t hh = p.rot / 2;
+    for (int vw = 8; vw >= 2; vw >>= 1) {
+        if (hh % vw) continue;
+        if ((p.Hq > 0 && (p.sq_b % vw || p.sq_s % vw || p.sq_h % vw || !aligned(p.q, 2 * vw))) ||
+            (p.Hk > 0 && (p.sk_b % vw || p.sk_s % vw || p.sk_h % vw || !aligned(p.k, 2 * vw))))
+            continue;
+        if (!p.freqs && (!aligned(p.cos, 2 * vw) || !aligned(p.sin, 2 * vw))) continue;
+        return vw;
+    }
+    return 1;
+}
+
+template <int VW, bool ANGLES>
+cudaError_t launch_qk_fast(const QKArgs& a, cudaStream_t st) {
+    const int64_t ntok = a.p.B * a.p.S;
+    int64_t blocks = (ntok + kWarps - 1) / kWarps;
+    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    rope_qk_kernel<VW, 4, ANGLES><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool ANGLES>
+cudaError_t launch_qk(const RopeQKParams& p, cudaStream_t st) {
+    const int vw = pick_qk_vw(p);
+    const int64_t hh = p.rot / 2;
+    if (vw >= 2 && hh / vw <= 32 && (!ANGLES || p.rot <= kMaxRot)) {
+        QKArgs a;
+        a.p = p;
+        a.NP = (int)(hh / vw);
+        a.RPW = 32 / a.NP;
+        switch (vw) {
+            case 8: return launch_qk_fast<8, ANGLES>(a, st);
+            case 4: return launch_qk_fast<4, ANGLES>(a, st);
+            default: return launch_qk_fast<2, ANGLES>(a, st);
+        }
+    }
+    const int64_t total = p.B * p.S * (p.Hq + p.Hk) * hh;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    rope_qk_generic_kernel<ANGLES><<<(unsigned)blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rope_qk(const RopeQKParams& p, cudaStream_t st) {
+    return p.freqs ? launch_qk<true>(p, st) : launch_qk<false>(p, st);
+}
+
+}  // namespace dtrot

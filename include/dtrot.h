@@ -109,6 +109,36 @@ dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int64_t S, int
                                     int64_t so_s, int64_t so_h, void* stream);
 
 /*
+ * Rotate-half RoPE on q and k in one launch, in place.   [P4] sections 1-2
+ *
+ * Applies the rotation of dtrot_rope_rotate_half to every head row of q and of
+ * k, overwriting them; tail columns [rot_dim, D) are not touched.  The cos/sin
+ * row of token (b, s) comes either from the tables (cos, sin, as written by
+ * dtrot_rope_cos_sin_precompute) or, when `freqs` is given instead, is
+ * evaluated from the angles inside the kernel with the same result as the
+ * table kernel (bit for bit) and is never stored.
+ *   q         bf16, (B, S, Hq, D), element strides (sq_b, sq_s, sq_h), D
+ *             contiguous.  May be NULL when Hq == 0.
+ *   k         bf16, (B, S, Hk, D), strides (sk_b, sk_s, sk_h).  May be NULL
+ *             when Hk == 0.  q and k must not share elements: either their
+ *             byte ranges are disjoint, or they are the two head ranges of one
+ *             (B, S, Hq + Hk, D) view (equal strides, the second starting
+ *             where the first one's heads end, as the q and k parts of a fused
+ *             QKV buffer are); else DTROT_ERR_ALIAS.  Each must have
+ *             non-overlapping rows (DTROT_ERR_STRIDE).
+ *   cos, sin  bf16, (B*S, rot_dim) contiguous, or both NULL when freqs is given.
+ *   freqs     fp32, (S, B, 1, rot_dim) contiguous, or NULL when tables are
+ *             given.  Giving both is DTROT_ERR_VALUE; neither, DTROT_ERR_NULL.
+ *             Tables or angles must not overlap q or k (DTROT_ERR_ALIAS).
+ *   rot_dim   even, 0 < rot_dim <= D (else DTROT_ERR_ROTDIM).
+ */
+dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_t sq_b, int64_t sq_s,
+                                       int64_t sq_h, uint16_t* k, int64_t Hk, int64_t sk_b,
+                                       int64_t sk_s, int64_t sk_h, int64_t B, int64_t S,
+                                       int64_t D, const uint16_t* cos, const uint16_t* sin,
+                                       const float* freqs, int64_t rot_dim, void* stream);
+
+/*
  * Bytes of device workspace dtrot_gelu_and_mul needs (its activation table:
  * 65536 bf16 entries, 131072 bytes).  Constant for a given library version.
  */

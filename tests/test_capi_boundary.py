@@ -33,7 +33,8 @@ def declared_functions():
 
 def test_header_declares_the_four_ops():
     names = declared_functions()
-    for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half", "dtrot_gelu_and_mul",
+    for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half",
+               "dtrot_rope_rotate_half_qk", "dtrot_gelu_and_mul",
                "dtrot_gelu_and_mul_workspace_bytes", "dtrot_rmsnorm_residual",
                "dtrot_status_str", "dtrot_version"):
         assert op in names
@@ -90,6 +91,43 @@ def tables(**kw):
     a.update(kw)
     return _capi.call("dtrot_rope_cos_sin_precompute", a["f"], a["S"], a["B"], a["R"], a["c"],
                       a["s"], None)
+
+
+def rope_qk(**kw):
+    # q heads [0, 2) and k heads [2, 4) of one (1, 4, 6, 8) QKV buffer at P
+    a = dict(q=P, Hq=2, sq_b=192, sq_s=48, sq_h=8, k=P + 2 * 16, Hk=2, sk_b=192, sk_s=48, sk_h=8,
+             B=1, S=4, D=8, cos=Q, sin=R, freqs=0, rot=8)
+    a.update(kw)
+    return _capi.call("dtrot_rope_rotate_half_qk", a["q"], a["Hq"], a["sq_b"], a["sq_s"],
+                      a["sq_h"], a["k"], a["Hk"], a["sk_b"], a["sk_s"], a["sk_h"], a["B"],
+                      a["S"], a["D"], a["cos"] or None, a["sin"] or None, a["freqs"] or None,
+                      a["rot"], None)
+
+
+def test_rope_qk_validation(lib):
+    assert rope_qk(S=0, q=0, k=0, cos=0, sin=0) == _capi.OK
+    assert rope_qk(Hq=0, Hk=0) == _capi.OK
+    assert rope_qk(q=0) == _capi.ERR_NULL
+    assert rope_qk(Hq=0, q=0, k=P) in (_capi.ERR_DEVICE, _capi.OK)   # k alone
+    assert rope_qk(cos=0) == _capi.ERR_NULL
+    assert rope_qk(freqs=W) == _capi.ERR_VALUE                        # tables and angles
+    assert rope_qk(rot=6, D=4) == _capi.ERR_ROTDIM
+    assert rope_qk(rot=5) == _capi.ERR_ROTDIM
+    assert rope_qk(Hk=-1) == _capi.ERR_SHAPE
+    assert rope_qk(sq_h=0) == _capi.ERR_STRIDE
+    assert rope_qk(sk_h=4) == _capi.ERR_STRIDE                        # k rows overlap
+    assert rope_qk(k=P + 2 * 8) == _capi.ERR_ALIAS                    # k starts inside q
+    assert rope_qk(k=P + 2 * 16, sk_s=96) == _capi.ERR_ALIAS          # interleaved, other strides
+    assert rope_qk(cos=P) == _capi.ERR_ALIAS                          # tables over q
+    assert rope_qk(cos=0, sin=0, freqs=P + 2 * 40) == _capi.ERR_ALIAS  # angles over k
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host without a GPU only")
+def test_rope_qk_valid_layouts_reach_the_device_check(lib):
+    assert rope_qk() == _capi.ERR_DEVICE                               # fused QKV slices
+    assert rope_qk(q=P + 2 * 16, k=P) == _capi.ERR_DEVICE              # k heads before q heads
+    assert rope_qk(k=W, sk_b=64, sk_s=16) == _capi.ERR_DEVICE          # separate buffers
+    assert rope_qk(cos=0, sin=0, freqs=Q) == _capi.ERR_DEVICE          # angles
 
 
 def test_zero_sized_calls_are_noops(lib):

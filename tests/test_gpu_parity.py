@@ -174,6 +174,84 @@ def test_rope_empty():
     assert out.shape == x.shape
 
 
+# ---------------------------------------------------------------- q and k in one launch
+
+def _qk_check(B, S, Hq, Hk, D, rot, freqs, seed, mode, layout="qkv", offset=0):
+    """RoPE on q and k in place, in one launch, against the oracle on each."""
+    Hv = Hq if layout == "qkv" else 0
+    if layout == "qkv":
+        buf = W.normal_bf16((B, S, Hq + Hk + Hv, D), seed, 0)
+        dbuf = to_dev(buf)
+        if offset:
+            flat = torch.empty(dbuf.numel() + offset, dtype=torch.bfloat16, device=DEV)
+            view = flat[offset:].view(dbuf.shape)
+            view.copy_(dbuf)
+            dbuf = view
+        q, k, v = dbuf[:, :, :Hq], dbuf[:, :, Hq:Hq + Hk], dbuf[:, :, Hq + Hk:]
+        q0, k0 = bits(buf)[:, :, :Hq], bits(buf)[:, :, Hq:Hq + Hk]
+        v0 = bits(buf)[:, :, Hq + Hk:]
+    else:
+        qh = W.normal_bf16((B, S, Hq, D), seed, 0)
+        kh = W.normal_bf16((B, S, Hk, D), seed, 1)
+        q, k, v = to_dev(qh), to_dev(kh), None
+        q0, k0 = bits(qh), bits(kh)
+    ec, es = oracle.rope_cos_sin(freqs.numpy())
+    if mode == "angles":
+        dt.rope_rotate_half_qk_(q, k, freqs=to_dev(freqs))
+    else:
+        dt.rope_rotate_half_qk_(q, k, cos=to_dev(from_u16(ec)), sin=to_dev(from_u16(es)))
+    torch.cuda.synchronize()
+    assert_bitexact(bits(q), oracle.rope_rotate_half(q0, ec, es), f"q {mode}")
+    assert_bitexact(bits(k), oracle.rope_rotate_half(k0, ec, es), f"k {mode}")
+    if v is not None:
+        assert_bitexact(bits(v), v0, "v untouched")
+
+
+@pytest.mark.parametrize("mode", ["tables", "angles"])
+@pytest.mark.parametrize("name", ["tiny", "image", "cfg"])
+def test_rope_qk_fused_qkv_configs(name, mode):
+    wl = W.WORKLOADS[name]
+    _qk_check(wl.B, wl.S, wl.H, wl.H, wl.D, wl.rot, W.freqs_for(wl), wl.seed + 50, mode)
+
+
+@pytest.mark.parametrize("mode", ["tables", "angles"])
+@pytest.mark.parametrize("D,rot", SWEEP)
+def test_rope_qk_sweep_odd_S_gqa(D, rot, mode):
+    B, S = 1, 4097
+    _qk_check(B, S, 6, 2, D, rot, W.freqs_1d(S, B, rot), 90 + D + rot, mode)
+
+
+@pytest.mark.parametrize("mode", ["tables", "angles"])
+def test_rope_qk_separate_buffers_misaligned_and_wide(mode):
+    _qk_check(2, 37, 3, 5, 128, 96, W.freqs_1d(37, 2, 96), 7, mode, layout="separate")
+    _qk_check(2, 37, 3, 3, 128, 96, W.freqs_1d(37, 2, 96), 8, mode, offset=1)  # scalar path
+    _qk_check(1, 19, 2, 2, 640, 576, W.freqs_1d(19, 1, 576), 9, mode)          # rot > 256
+
+
+def test_rope_qk_special_angles_match_the_table_kernel():
+    g = torch.Generator().manual_seed(23)
+    f = torch.empty(64 * 32, dtype=torch.float32).uniform_(-300.0, 300.0, generator=g)
+    special = torch.tensor([0.0, -0.0, 1e-30, 1.5707964, 3.1415927, 1e4, -3.3e4, 1e6, 1e30,
+                            float("inf"), float("-inf"), float("nan")])
+    f[:special.numel()] = special
+    freqs = f.view(64, 1, 1, 32)
+    _qk_check(1, 64, 2, 2, 32, 32, freqs, 10, "angles")
+
+
+def test_rope_qk_video_full_size_sampled_tokens():
+    wl = W.WORKLOADS["video"]
+    q, k = W.rope_inputs(wl, "q"), W.rope_inputs(wl, "k")
+    freqs = W.freqs_for(wl)
+    dq, dk = to_dev(q), to_dev(k)
+    dt.rope_rotate_half_qk_(dq, dk, freqs=to_dev(freqs))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    toks = np.unique(np.concatenate([[0, wl.S - 1], rng.choice(wl.S, 512, replace=False)]))
+    ec, es = oracle.rope_cos_sin(freqs.numpy()[toks])
+    assert_bitexact(bits(dq)[:, toks], oracle.rope_rotate_half(bits(q)[:, toks], ec, es), "q")
+    assert_bitexact(bits(dk)[:, toks], oracle.rope_rotate_half(bits(k)[:, toks], ec, es), "k")
+
+
 # ---------------------------------------------------------------- a3 GEGLU
 
 def test_geglu_every_bf16_gate_value_bitexact():
