@@ -5,6 +5,7 @@ rotary cos/sin tables, rotate-half RoPE, GEGLU with activation rounding, and
 RMSNorm fused with the residual add.  The torch wrappers in `api` only pass
 pointers, sizes and strides; `_capi` is the raw ctypes binding.
 """
+from . import selfcheck  # noqa: F401
 from ._capi import DtrotError, DtrotUnavailable, load  # noqa: F401
 from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_workspace,  # noqa: F401
                   rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half,

@@ -21,6 +21,7 @@ import threading
 import torch
 
 from . import _capi
+from . import selfcheck as _sc
 
 _ws_lock = threading.Lock()
 _ws_cache: dict = {}
@@ -63,6 +64,10 @@ def rope_cos_sin_precompute(freqs: torch.Tensor, cos_out: torch.Tensor | None = 
             raise ValueError(f"{n} must be contiguous (B*S, R)")
     _capi.check("dtrot_rope_cos_sin_precompute", freqs.data_ptr(), S, B, R, cos_out.data_ptr(),
                 sin_out.data_ptr(), _stream(freqs))
+    if _sc.want("rope_cos_sin_precompute", freqs):
+        rc, rs = _sc.ref_tables(freqs)
+        _sc.compare("rope_cos_sin_precompute cos", cos_out, rc, exact=False)
+        _sc.compare("rope_cos_sin_precompute sin", sin_out, rs, exact=False)
     return cos_out, sin_out
 
 
@@ -88,9 +93,13 @@ def rope_rotate_half(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
         raise ValueError("out must have the shape of x")
     _last_contiguous(out, "out")
     sx, so = x.stride(), out.stride()
+    key = _sc.want("rope_rotate_half", x, cos)
+    x0 = x.clone() if key else None
     _capi.check("dtrot_rope_rotate_half", x.data_ptr(), B, S, H, D, sx[0], sx[1], sx[2],
                 cos.data_ptr(), sin.data_ptr(), rot, out.data_ptr(), so[0], so[1], so[2],
                 _stream(x))
+    if key:
+        _sc.compare("rope_rotate_half", out, _sc.ref_rope(x0, cos, sin), exact=True)
     return out
 
 
@@ -130,9 +139,16 @@ def rope_rotate_half_qk_(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | N
         rot = cos.shape[1]
         cp, sp, fp = cos.data_ptr(), sin.data_ptr(), 0
     sq, sk = q.stride(), k.stride()
+    key = _sc.want("rope_rotate_half_qk", q, k, cos if freqs is None else freqs)
+    q0, k0 = (q.clone(), k.clone()) if key else (None, None)
     _capi.check("dtrot_rope_rotate_half_qk", q.data_ptr(), Hq, sq[0], sq[1], sq[2],
                 k.data_ptr(), Hk, sk[0], sk[1], sk[2], B, S, D, cp or None, sp or None,
                 fp or None, rot, _stream(q))
+    if key:
+        if freqs is not None:
+            cos, sin = _sc.ref_tables(freqs)
+        _sc.compare("rope_rotate_half_qk q", q, _sc.ref_rope(q0, cos, sin), exact=True)
+        _sc.compare("rope_rotate_half_qk k", k, _sc.ref_rope(k0, cos, sin), exact=True)
 
 
 def _rows(t: torch.Tensor, name: str):
@@ -178,8 +194,12 @@ def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor, out: torch.Tensor | None 
     elif not workspace.is_cuda:
         raise ValueError("workspace must be a CUDA tensor")
     nbytes = workspace.numel() * workspace.element_size()
+    key = _sc.want("gelu_and_mul", gate, up)
+    ref = _sc.ref_geglu(gate, up) if key else None
     _capi.check("dtrot_gelu_and_mul", gate.data_ptr(), sg, up.data_ptr(), su, out.data_ptr(),
                 so, T, F, workspace.data_ptr(), nbytes, st)
+    if key:
+        _sc.compare("gelu_and_mul", out, ref, exact=False)
     return out
 
 
@@ -211,6 +231,11 @@ def rmsnorm_residual(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor,
         out = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
     _need(out, "out", torch.bfloat16)
     so = _rows(out, "out")
+    key = _sc.want("rmsnorm_residual", x, w)
+    ref = _sc.ref_rmsnorm(x, residual, w, eps) if key else None
     _capi.check("dtrot_rmsnorm_residual", x.data_ptr(), sx, residual.data_ptr(), sr,
                 w.data_ptr(), float(eps), out.data_ptr(), so, T, C, _stream(x))
+    if key:
+        _sc.compare("rmsnorm_residual residual", residual, ref[0], exact=True)
+        _sc.compare("rmsnorm_residual out", out, ref[1], exact=False)
     return out
