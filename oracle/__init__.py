@@ -18,6 +18,11 @@ Functions and the passages they follow:
                      to bf16 before the multiply).
   rmsnorm_residual   sequence-parallelism post, per-token RMSNorm and residual
                      add, Pre-Norm order (add, then normalise).
+  gate_up_bf16       same ERNIE-Image page, section 3 (the MLP's gate_up
+                     projection feeding GEGLU): x W^T rounded to bf16, with
+                     bounds for an fp32 accumulation in any order.
+  gemm_gelu_and_mul  gate_up_bf16 followed by gelu_and_mul (gate = first F
+                     output features).
   *_f64              the same row formulas with every rounding removed, used by
                      the invariant pins (norm preservation, relative position,
                      unit RMS).
@@ -69,6 +74,8 @@ def lib():
         L.dto_rmsnorm_residual_f64.argtypes = [_p, _p, _p, ctypes.c_double, _p, _p,
                                                _i64, _i64]
         L.dto_rmsnorm_residual_f64.restype = None
+        L.dto_gate_up_bf16.argtypes = [_p, _i64, _i64, _p, _i64, ctypes.c_double, _p, _p, _p]
+        L.dto_gate_up_bf16.restype = None
         L.dto_num_threads.argtypes = []
         L.dto_num_threads.restype = ctypes.c_int
         if not L.dto_fp_env_ok():
@@ -246,3 +253,30 @@ def rmsnorm_residual_f64(x, residual, w, eps):
     lib().dto_rmsnorm_residual_f64(_ptr(x), _ptr(r), _ptr(w), float(eps), _ptr(h), _ptr(y),
                                    T, C)
     return h, y
+
+
+# ---------------------------------------------------------------- gate_up projection + GEGLU
+
+def gate_up_bf16(x: np.ndarray, w: np.ndarray, eps: float = 0.0):
+    """x uint16 (T, C), w uint16 (N, C) -> (exact, lo, hi) uint16 (T, N): the
+    bf16 rounding of x W^T, and the roundings of its ends when each dot product
+    may be off by eps * sum|x w| (an fp32 accumulation in any order)."""
+    x = np.ascontiguousarray(_u16(x))
+    w = np.ascontiguousarray(_u16(w))
+    T, C = x.shape
+    N = w.shape[0]
+    if w.shape[1] != C:
+        raise ValueError("x is (T, C) and w is (N, C)")
+    exact = np.empty((T, N), dtype=np.uint16)
+    lo = np.empty((T, N), dtype=np.uint16)
+    hi = np.empty((T, N), dtype=np.uint16)
+    lib().dto_gate_up_bf16(_ptr(x), T, C, _ptr(w), N, float(eps), _ptr(exact), _ptr(lo),
+                           _ptr(hi))
+    return exact, lo, hi
+
+
+def gemm_gelu_and_mul(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """GEGLU of the bf16 gate_up projection: w (2F, C), gate rows first."""
+    gu, _, _ = gate_up_bf16(x, w)
+    F = w.shape[0] // 2
+    return gelu_and_mul(gu[:, :F], gu[:, F:])

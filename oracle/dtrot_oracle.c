@@ -273,6 +273,42 @@ EXPORT void dto_rmsnorm_residual_f64(const double* x, const double* residual,
         rmsnorm_row(x + t * C, residual + t * C, w, eps, C, 1, h_out + t * C, y_out + t * C);
 }
 
+/* ------------------------------------------------------------------ */
+/* GEGLU after the gate_up projection (ERNIE-Image page, section 3)    */
+/* ------------------------------------------------------------------ */
+
+/* The MLP's gate_up = x W^T, with x (T, C) and W (N, C) bf16 (an nn.Linear
+ * weight, output features in rows; for GEGLU N = 2F, gate rows first), is a
+ * bf16 tensor: the exact dot products rounded once to bf16.  Each product of
+ * two bf16 values is exact in double and the sum of C of them carries an error
+ * below C * 2^-53 of the sum of magnitudes, far inside any rounding question
+ * this file decides.  For the bounds used when the sum is accumulated in fp32
+ * (in any order), also returns, per element,
+ *   lo = RN16(dot - eps * sum|x w|),  hi = RN16(dot + eps * sum|x w|):
+ * every fp32 accumulation whose error is below eps * sum|x w| rounds to a bf16
+ * value between lo and hi. */
+EXPORT void dto_gate_up_bf16(const uint16_t* x, int64_t T, int64_t C, const uint16_t* w,
+                             int64_t N, double eps, uint16_t* exact, uint16_t* lo,
+                             uint16_t* hi) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double* xr = (double*)malloc(sizeof(double) * (size_t)(C + 1));
+        for (int64_t c = 0; c < C; ++c) xr[c] = dto_bf16_to_double(x[t * C + c]);
+        for (int64_t n = 0; n < N; ++n) {
+            double dot = 0.0, mag = 0.0;
+            for (int64_t c = 0; c < C; ++c) {
+                double p = xr[c] * dto_bf16_to_double(w[n * C + c]);
+                dot += p;
+                mag += fabs(p);
+            }
+            exact[t * N + n] = dto_rn16(dot);
+            if (lo) lo[t * N + n] = dto_rn16(dot - eps * mag);
+            if (hi) hi[t * N + n] = dto_rn16(dot + eps * mag);
+        }
+        free(xr);
+    }
+}
+
 /* Threads the OpenMP loops use (reported beside the CPU timings). */
 #ifdef _OPENMP
 #include <omp.h>
