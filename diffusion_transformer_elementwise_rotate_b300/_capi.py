@@ -23,9 +23,10 @@ STATUS = {
     7: "DTROT_ERR_DEVICE",
     8: "DTROT_ERR_VALUE",
     9: "DTROT_ERR_WORKSPACE",
+    10: "DTROT_ERR_ALIGN",
 }
 OK, ERR_NULL, ERR_SHAPE, ERR_ROTDIM, ERR_STRIDE, ERR_ALIAS, ERR_LAUNCH, ERR_DEVICE, \
-    ERR_VALUE, ERR_WORKSPACE = range(10)
+    ERR_VALUE, ERR_WORKSPACE, ERR_ALIGN = range(11)
 
 # entry point -> (restype, argtypes); must match include/dtrot.h
 _i64 = ctypes.c_int64
@@ -43,6 +44,9 @@ SIGNATURES = {
     "dtrot_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
     "dtrot_gelu_and_mul": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p, _i64,
                                           _p]),
+    "dtrot_gemm_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
+    "dtrot_gemm_gelu_and_mul": (ctypes.c_int, [_p, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
+                                               _p, _i64, _p]),
     "dtrot_gelu_and_mul_noalloc": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p]),
     "dtrot_rmsnorm_residual": (ctypes.c_int,
                                [_p, _i64, _p, _i64, _p, ctypes.c_float, _p, _i64, _i64, _i64,

@@ -11,6 +11,8 @@ runs in libdtrot's sm_103a kernels.
                                          tables, or angles evaluated in the kernel
   gelu_and_mul(gate, up, out=None, workspace=None) -> out     ERNIE-Image page, section 3
   gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
+  gemm_gelu_and_mul(x, w, out=None, workspace=None) -> out   GEGLU in the epilogue of the
+                                         gate_up projection x w^T (tcgen05 tensor cores)
   rmsnorm_residual(x, residual, w, eps=1e-6, out=None) -> out   (residual updated in place)
                                                          sequence-parallelism post
 """
@@ -200,6 +202,59 @@ def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor, out: torch.Tensor | None 
                 so, T, F, workspace.data_ptr(), nbytes, st)
     if key:
         _sc.compare("gelu_and_mul", out, ref, exact=False)
+    return out
+
+
+def _cached_workspace(kind: str, query: str, device: torch.device, stream: int) -> torch.Tensor:
+    key = (kind, torch.device(device).index, int(stream))
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None:
+            n = int(getattr(_capi.load(), query)())
+            ws = torch.empty(n, dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+    return ws
+
+
+def gemm_gelu_and_mul(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None,
+                      gate_up: torch.Tensor | None = None) -> torch.Tensor:
+    """GEGLU of the MLP's gate_up projection without storing gate_up:
+    x bf16 (T, C), w bf16 (2F, C) (gate rows first) -> out bf16 (T, F) =
+    up * gelu(gate) with gate_up = x w^T rounded to bf16.  If `gate_up` (bf16
+    (T, 2F)) is given, the rounded projection is stored there as well."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    if x.dim() != 2 or w.dim() != 2 or w.shape[1] != x.shape[1] or w.shape[0] % 2:
+        raise ValueError("x must be (T, C) and w (2F, C)")
+    if not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous")
+    T, C = x.shape
+    F = w.shape[0] // 2
+    if out is None:
+        out = torch.empty((T, F), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16)
+    if out.shape != (T, F):
+        raise ValueError("out must be (T, F)")
+    so = _rows(out, "out")
+    st = _stream(x)
+    if workspace is None:
+        workspace = _cached_workspace("gemm_geglu", "dtrot_gemm_gelu_and_mul_workspace_bytes",
+                                      x.device, st)
+    gp, sgu = 0, 2 * F
+    if gate_up is not None:
+        _need(gate_up, "gate_up", torch.bfloat16)
+        if gate_up.shape != (T, 2 * F):
+            raise ValueError("gate_up must be (T, 2F)")
+        gp, sgu = gate_up.data_ptr(), _rows(gate_up, "gate_up")
+    key = _sc.want("gemm_gelu_and_mul", x, w)
+    _capi.check("dtrot_gemm_gelu_and_mul", x.data_ptr(), T, C, w.data_ptr(), F, out.data_ptr(),
+                so, gp or None, sgu, workspace.data_ptr(),
+                workspace.numel() * workspace.element_size(), st)
+    if key:
+        gu = (x.double() @ w.double().t()).float().to(torch.bfloat16)
+        _sc.compare("gemm_gelu_and_mul", out, _sc.ref_geglu(gu[:, :F], gu[:, F:]), exact=False,
+                    max_fraction=1e-2)
     return out
 
 

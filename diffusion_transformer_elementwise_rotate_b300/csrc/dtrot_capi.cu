@@ -177,6 +177,8 @@ DTROT_API const char* dtrot_status_str(dtrot_status s) {
         case DTROT_ERR_VALUE: return "DTROT_ERR_VALUE: a scalar argument is out of range";
         case DTROT_ERR_WORKSPACE:
             return "DTROT_ERR_WORKSPACE: the workspace is too small or not 16-byte aligned";
+        case DTROT_ERR_ALIGN:
+            return "DTROT_ERR_ALIGN: a pointer, stride or size misses the op's alignment";
     }
     return "DTROT_ERR_UNKNOWN";
 }
@@ -410,6 +412,66 @@ DTROT_API dtrot_status dtrot_gelu_and_mul_noalloc(const uint16_t* gate, int64_t 
     if (gelu_table_bytes() > capacity) return DTROT_ERR_WORKSPACE;
     return dtrot_gelu_and_mul(gate, s_gate, up, s_up, out, s_out, T, F, table,
                               (int64_t)capacity, stream);
+}
+
+DTROT_API int64_t dtrot_gemm_gelu_and_mul_workspace_bytes(void) {
+    return (int64_t)gemm_geglu_workspace_bytes();
+}
+
+DTROT_API dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int64_t C,
+                                               const uint16_t* w, int64_t F, uint16_t* out,
+                                               int64_t s_out, uint16_t* gate_up,
+                                               int64_t s_gate_up, void* workspace,
+                                               int64_t workspace_bytes, void* stream) {
+    if (T < 0 || C < 0 || F < 0) return DTROT_ERR_SHAPE;
+    int64_t n, f2, nw;
+    if (!mul_ok(T, C, &n) || !mul_ok(n, 2, &n) || !mul_ok(F, 2, &f2) || !mul_ok(f2, C, &nw) ||
+        !mul_ok(nw, 2, &nw) || !mul_ok(T, F, &n) || !mul_ok(n, 2, &n))
+        return DTROT_ERR_SHAPE;
+    if (T == 0 || F == 0) return DTROT_OK;
+    if (C == 0) return DTROT_ERR_SHAPE;  // no projection to take
+    if (T > 0x7FFFFFFF || f2 > 0x7FFFFFFF) return DTROT_ERR_SHAPE;
+    if (!x || !w || !out || !workspace) return DTROT_ERR_NULL;
+    if (T > 1 && (s_out < F || (gate_up && s_gate_up < 2 * F))) return DTROT_ERR_STRIDE;
+    const int64_t so = T > 1 ? s_out : F;
+    const int64_t sg = T > 1 ? s_gate_up : 2 * F;
+    if (C % 8 || F % 8 || so % 8 || (uintptr_t)x % 16 || (uintptr_t)w % 16 ||
+        (uintptr_t)out % 16 || (gate_up && (sg % 8 || (uintptr_t)gate_up % 16)))
+        return DTROT_ERR_ALIGN;
+    if (workspace_bytes < (int64_t)gemm_geglu_workspace_bytes() || (uintptr_t)workspace % 16)
+        return DTROT_ERR_WORKSPACE;
+    {
+        int64_t size[2] = {T, F}, st[2] = {so, 1};
+        Range ro;
+        if (!span(out, 2, size, st, 2, &ro)) return DTROT_ERR_SHAPE;
+        const Range rx{(uintptr_t)x, (uintptr_t)x + (uintptr_t)(T * C * 2)};
+        const Range rw{(uintptr_t)w, (uintptr_t)w + (uintptr_t)nw};
+        const Range rws{(uintptr_t)workspace,
+                        (uintptr_t)workspace + (uintptr_t)gemm_geglu_workspace_bytes()};
+        if (overlap(ro, rx) || overlap(ro, rw) || overlap(ro, rws) || overlap(rws, rx) ||
+            overlap(rws, rw))
+            return DTROT_ERR_ALIAS;
+        if (gate_up) {
+            int64_t gsize[2] = {T, 2 * F}, gst[2] = {sg, 1};
+            Range rg;
+            if (!span(gate_up, 2, gsize, gst, 2, &rg)) return DTROT_ERR_SHAPE;
+            if (overlap(rg, rx) || overlap(rg, rw) || overlap(rg, rws) || overlap(rg, ro))
+                return DTROT_ERR_ALIAS;
+        }
+    }
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    GemmGegluArgs a;
+    a.x = x;
+    a.w = w;
+    a.T = T;
+    a.C = C;
+    a.F = F;
+    a.out = out;
+    a.s_out = so;
+    a.gate_up = gate_up;
+    a.s_gate_up = sg;
+    a.workspace = workspace;
+    return launch_status(launch_gemm_geglu(a, (cudaStream_t)stream));
 }
 
 DTROT_API dtrot_status dtrot_rmsnorm_residual(const uint16_t* x, int64_t sx, uint16_t* residual,

@@ -107,6 +107,34 @@ __device__ __forceinline__ void cos_sin_entry(float f, uint16_t& c16, uint16_t& 
     s16 = rn16f(s32);
 }
 
+// ------------------------------------------------------------ GELU table entries
+
+// RN16(RN32(gelu(x))) for the bf16 value with bit pattern `bits`, gelu(x) =
+// x/2 * erfc(-x/sqrt 2) (the erf form's exact equal, without its cancellation
+// for x << 0).  fp32 erfcf decides the rounding unless the fp32 value lies
+// within an error margin of a bf16 rounding midpoint (the margin grows with
+// erfc's condition number 2z^2 for z = -x/sqrt 2 > 0); those entries, and the
+// far negative tail x in (-20, -9) where the fp32 erfc result loses precision
+// to underflow, are recomputed in fp64 and rounded to fp32, then to bf16.
+__device__ inline uint16_t gelu_entry(uint32_t bits) {
+    const float x = __uint_as_float(bits << 16);
+    const float z = __fmul_rn(x, -0.70710678118654752440f);  // -x / sqrt 2
+    bool slow = (x < -9.0f) && (x > -20.0f);
+    float y = 0.0f;
+    if (!slow) {
+        const float e = erfcf(z);
+        y = __fmul_rn(__fmul_rn(0.5f, x), e);
+        const float zz = z > 0.0f ? fminf(z, 16.0f) : 0.0f;
+        const int margin = 8 + (int)(4.0f * zz * zz);
+        slow = ulps_to_bf16_midpoint(y) <= margin;
+    }
+    if (slow) {
+        const double xd = (double)x;
+        y = __double2float_rn(0.5 * xd * erfc(-xd * 0.70710678118654752440));
+    }
+    return rn16f(y);
+}
+
 // ------------------------------------------------------------ launchers
 
 struct RopeParams {
@@ -131,6 +159,17 @@ struct RopeQKParams {
     int64_t sk_b, sk_s, sk_h;
 };
 
+struct GemmGegluArgs {
+    const uint16_t* x;   // (T, C) row-major
+    const uint16_t* w;   // (2F, C) row-major, gate rows first
+    int64_t T, C, F;
+    uint16_t* out;       // (T, F), row stride s_out
+    int64_t s_out;
+    uint16_t* gate_up;   // optional (T, 2F), row stride s_gate_up
+    int64_t s_gate_up;
+    void* workspace;     // gemm_geglu_workspace_bytes()
+};
+
 struct GegluParams {
     const uint16_t* gate;
     const uint16_t* up;
@@ -153,6 +192,8 @@ cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_
                                 uint16_t* cos_out, uint16_t* sin_out, cudaStream_t st);
 cudaError_t launch_rope_rotate_half(const RopeParams& p, cudaStream_t st);
 cudaError_t launch_rope_qk(const RopeQKParams& p, cudaStream_t st);
+size_t gemm_geglu_workspace_bytes();
+cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st);
 size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);
 // Device address and size of the library-owned activation table of the

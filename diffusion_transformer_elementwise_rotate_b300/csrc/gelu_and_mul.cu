@@ -17,11 +17,8 @@
 // paid 65536 times per call instead of once per element, and the result is
 // the exactly rounded GELU.
 //
-// Table entries: fp32 erfcf decides the rounding unless the fp32 value lies
-// within an error margin of a bf16 rounding midpoint (the margin grows with
-// erfc's condition number 2z^2 for z = -x/sqrt 2 > 0); those entries, and the
-// far negative tail x in (-20, -9) where the fp32 erfc result loses precision
-// to underflow, are recomputed in fp64 and rounded to fp32, then to bf16.
+// Table entries: gelu_entry (shared with the GEGLU epilogue of the gate_up
+// projection).
 #include <atomic>
 
 #include "dtrot_internal.cuh"
@@ -31,25 +28,6 @@ namespace {
 
 constexpr int kTable = 1 << 16;
 constexpr int kThreads = 1024;
-
-__device__ uint16_t gelu_entry(uint32_t bits) {
-    const float x = __uint_as_float(bits << 16);
-    const float z = __fmul_rn(x, -0.70710678118654752440f);  // -x / sqrt 2
-    bool slow = (x < -9.0f) && (x > -20.0f);
-    float y = 0.0f;
-    if (!slow) {
-        const float e = erfcf(z);
-        y = __fmul_rn(__fmul_rn(0.5f, x), e);
-        const float zz = z > 0.0f ? fminf(z, 16.0f) : 0.0f;
-        const int margin = 8 + (int)(4.0f * zz * zz);
-        slow = ulps_to_bf16_midpoint(y) <= margin;
-    }
-    if (slow) {
-        const double xd = (double)x;
-        y = __double2float_rn(0.5 * xd * erfc(-xd * 0.70710678118654752440));
-    }
-    return rn16f(y);
-}
 
 __device__ __forceinline__ uint32_t lookup2(const uint16_t* tab, uint32_t g) {
     const uint32_t lo = tab[g & 0xFFFFu];

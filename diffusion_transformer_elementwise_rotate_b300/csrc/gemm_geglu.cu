@@ -1,0 +1,458 @@
+// GEGLU applied in the epilogue of the MLP's gate_up projection:
+//   gate_up = RN16(x W^T)        x (T, C), W (2F, C) bf16, fp32 accumulation
+//   out     = RN16(up * RN16(RN32(gelu(gate))))   gate = first F columns
+//
+// ERNIE-Image fusion page (sglang PR #34306 analysis), section 3: the MLP runs
+// gate_up_proj and then the fused GEGLU; the eager path wrote gate_up to HBM
+// and made two more passes over it.  Here the activation is applied to the
+// projection's accumulators before anything is stored, so gate_up never
+// reaches HBM: the call reads x and W and writes out.
+//
+// Design (one CTA per 128 x 128 output tile, tcgen05 tensor cores):
+//   - the B operand of a tile is 256 weight rows: gate rows f0..f0+127 and up
+//     rows F+f0..F+f0+127, so one 128 x 256 fp32 accumulator in tensor memory
+//     holds gate and up of the same 128 output columns;
+//   - a kStages-deep ring of shared-memory stages (x: 128 x 64, W: 256 x 64
+//     bf16, 128-byte swizzle) filled by TMA (one thread) and consumed by
+//     tcgen05.mma (one thread, M 128, N 256, K 16 per instruction), with
+//     mbarriers for "stage full" (TMA transaction bytes) and "stage empty"
+//     (tcgen05.commit);
+//   - epilogue: each of the 4 warps reads its 32 accumulator lanes (rows) with
+//     tcgen05.ld, rounds gate and up to bf16 (the projection's output
+//     rounding), looks the activation up in a compact 17 KB table in shared
+//     memory and multiplies with one bf16x2 .rn multiply, as the standalone
+//     GEGLU kernel does;
+//   - optionally the rounded gate and up are stored too (a (T, 2F) gate_up
+//     tensor, for a backward pass or for checking);
+//   - tiles are visited in groups of 16 row tiles so that the x and W tiles a
+//     wave of CTAs reads stay in L2.
+// Every mbarrier wait is bounded (about a second of %globaltimer): a wait that
+// runs out records a code in the workspace's error word and the CTA finishes
+// without further waits; later CTAs that see the word set exit at once.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "dtrot_internal.cuh"
+
+namespace dtrot {
+namespace {
+
+constexpr int BM = 128;             // output rows per tile
+constexpr int BNH = 128;            // output columns per tile (gate or up half)
+constexpr int BN = 2 * BNH;         // MMA N: gate and up columns
+constexpr int BK = 64;              // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreads = 128;
+constexpr int kGroupM = 16;
+constexpr uint32_t kATile = BM * BK * 2;   // 16 KB
+constexpr uint32_t kBTile = BN * BK * 2;   // 32 KB
+constexpr uint32_t kStageBytes = kATile + kBTile;
+constexpr uint32_t kTmemCols = 256;
+
+// Compact activation table: entries for |x| in [2^-30, 8) (x > 0) and
+// [2^-30, 16) (x < 0), i.e. bf16 exponent fields 97..129 and 97..130; every
+// other gate value has a closed form (see gelu_lookup).
+constexpr int kExpLo = 97;
+constexpr int kPosEntries = (129 - kExpLo + 1) * 128;          // 4224
+constexpr int kCompact = kPosEntries + (130 - kExpLo + 1) * 128;  // 8576
+constexpr uint32_t kTabBytes = kCompact * 2;                   // 17152
+constexpr uint32_t kErrOffset = kTabBytes;                     // error word in the workspace
+constexpr uint32_t kWorkspaceBytes = 17408;
+
+constexpr uint32_t kErrTimeoutEmpty = 1, kErrTimeoutFull = 2, kErrTimeoutAccum = 4;
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any single wait
+
+struct GemmGegluParams {
+    uint16_t* out;
+    int64_t s_out;
+    uint16_t* gate_up;  // optional (T, 2F) copy of the rounded projection
+    int64_t s_gate_up;
+    int64_t T, C, F;
+    const uint16_t* table;  // compact activation table in the workspace
+    uint32_t* err;          // error word in the workspace
+    int num_m, num_n;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: false (and `code` recorded) when the phase did not complete in
+// kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err,
+                                          uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitNs) {
+            atomicOr(err, code);
+            return false;
+        }
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (start address and offsets in 16-byte units).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (not used with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// 32 consecutive fp32 accumulator columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_may_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- activation
+
+// g(x) = RN16(RN32(gelu(x))) for the bf16 pattern b, from the compact table or
+// a closed form:
+//   |x| < 2^-30 (exponent field < 97, zeros and subnormals included):
+//       gelu(x) = x/2 + x^2/sqrt(2 pi) + O(x^4) and x/2 is exact in fp32; the
+//       x^2 term is below 2^-25 |x/2|, so RN32 gives x/2 and g = RN16(x/2);
+//   x >= 8 (and +inf, NaN): gelu(x) = x (1 - erfc(x/sqrt 2)/2) differs from x
+//       by less than 2^-49 |x|, so RN32 gives x back;
+//   x <= -16: |gelu(x)| < 1e-55 < 2^-150, so RN32 gives -0; -inf gives NaN
+//       (-inf * 0) like the formula.
+__device__ __forceinline__ uint32_t gelu_lookup(const uint16_t* tab, uint32_t b) {
+    const uint32_t e = (b >> 7) & 0xFFu;
+    if (e < (uint32_t)kExpLo) return rn16f(__fmul_rn(__uint_as_float(b << 16), 0.5f));
+    if (!(b & 0x8000u)) return e >= 130 ? b : tab[(b & 0x7FFFu) - (kExpLo << 7)];
+    if (e >= 131) return e == 255 ? 0x7FC0u : 0x8000u;
+    return tab[kPosEntries + (b & 0x7FFFu) - (kExpLo << 7)];
+}
+
+__device__ __forceinline__ uint32_t gelu_lookup2(const uint16_t* tab, uint32_t g2) {
+    return gelu_lookup(tab, g2 & 0xFFFFu) | (gelu_lookup(tab, g2 >> 16) << 16);
+}
+
+// Compact table entry i (see kExpLo): the gelu_entry of its bf16 pattern.
+__global__ void __launch_bounds__(256) gelu_compact_table_kernel(uint16_t* __restrict__ table,
+                                                                 uint32_t* __restrict__ err) {
+    grid_dependents_may_launch();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i == 0) *err = 0;
+    if (i < kCompact) {
+        const uint32_t b = i < kPosEntries ? (uint32_t)(kExpLo << 7) + i
+                                           : 0x8000u | ((uint32_t)(kExpLo << 7) + (i - kPosEntries));
+        table[i] = gelu_entry(b);
+    }
+}
+
+// ---------------------------------------------------------------- the GEMM
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_geglu_kernel(const __grid_constant__ CUtensorMap tma_x,
+                      const __grid_constant__ CUtensorMap tma_w, GemmGegluParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_skip;
+    // the table kernel (the prerequisite grid) has written the activation table
+    // and cleared the error word once this returns; only CTAs that start while
+    // it still runs wait here
+    wait_for_prerequisite_grid();
+    // a CTA that starts after an earlier one ran out of a wait does nothing
+    // (decided by one thread, so the whole CTA leaves together)
+    if (threadIdx.x == 0) s_skip = *reinterpret_cast<volatile uint32_t*>(p.err);
+    __syncthreads();
+    if (s_skip != 0) return;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled tiles want 1024-byte alignment
+    uint8_t* sm = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + kStages * kATile;
+    uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStages * kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStages * kStageBytes + kTabBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStages;
+    const uint32_t accum = full0 + 16 * kStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // tile (grouped so a wave of CTAs shares x and W tiles in L2)
+    const int pid = blockIdx.x;
+    const int in_group = kGroupM * p.num_n;
+    const int first_m = (pid / in_group) * kGroupM;
+    const int gm = min(p.num_m - first_m, kGroupM);
+    const int m_t = first_m + (pid % in_group) % gm;
+    const int n_t = (pid % in_group) / gm;
+    const int m0 = m_t * BM, f0 = n_t * BNH;
+    const int nk = (int)((p.C + BK - 1) / BK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(accum, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(p.table);
+        uint4* dst = reinterpret_cast<uint4*>(tab);
+        for (int i = threadIdx.x; i < (int)(kTabBytes / 16); i += kThreads) dst[i] = __ldcg(src + i);
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // TMA producer
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+            if (kb >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1u, p.err, kErrTimeoutEmpty))
+                break;
+            const uint32_t fb = full0 + 8 * s;
+            mbar_expect_tx(fb, kStageBytes);
+            tma_load_2d(sA + s * kATile, &tma_x, kb * BK, m0, fb);
+            tma_load_2d(sB + s * kBTile, &tma_w, kb * BK, f0, fb);
+            tma_load_2d(sB + s * kBTile + BNH * BK * 2, &tma_w, kb * BK, (int32_t)p.F + f0, fb);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: 4 instructions of K 16 per stage, then the stage is
+        // released when they have read it
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+            if (!mbar_wait(full0 + 8 * s, ph, p.err, kErrTimeoutFull)) break;
+            tc_fence_after();
+            const uint64_t a = smem_desc(sA + s * kATile);
+            const uint64_t b = smem_desc(sB + s * kBTile);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+                mma_bf16(tmem, a + 2 * k, b + 2 * k, (kb | k) != 0 ? 1u : 0u);
+            mma_commit(empty0 + 8 * s);
+        }
+        mma_commit(accum);  // arrives once every MMA issued above has completed
+    }
+
+    const bool ok = mbar_wait(accum, 0, p.err, kErrTimeoutAccum);
+    __syncwarp();
+    tc_fence_after();
+    const int64_t row = (int64_t)m0 + warp * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int j = 0; j < BNH / 32; ++j) {
+        uint32_t g[32], u[32];
+        tmem_ld32(taddr + 32 * j, g);
+        tmem_ld32(taddr + BNH + 32 * j, u);
+        tmem_wait_ld();
+        if (ok && row < p.T) {
+            uint32_t o[16], gb[16], ub[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                gb[i] = rn16x2f(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                ub[i] = rn16x2f(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+                o[i] = bmul2(ub[i], gelu_lookup2(tab, gb[i]));
+            }
+            uint16_t* dst = p.out + row * p.s_out + f0 + 32 * j;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (f0 + 32 * j + 8 * q < p.F)
+                    *reinterpret_cast<uint4*>(dst + 8 * q) =
+                        make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
+            if (p.gate_up) {
+                uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (f0 + 32 * j + 8 * q < p.F) {
+                        *reinterpret_cast<uint4*>(gdst + 8 * q) =
+                            make_uint4(gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
+                        *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) =
+                            make_uint4(ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kStageBytes + kTabBytes + (2 * kStages + 1) * 8 + 16;
+
+constexpr int kMaxDev = 64;
+std::atomic<bool> g_smem_attr[kMaxDev];
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static std::atomic<EncodeTiled> fn{nullptr};
+    EncodeTiled f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !ptr)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiled>(ptr);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// 2-D bf16 tensor map over a (rows, cols) row-major matrix, boxes of 128 rows
+// x 64 columns, 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* m, const uint16_t* ptr, int64_t rows, int64_t cols) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {BK, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(ptr), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t gemm_geglu_workspace_bytes() { return kWorkspaceBytes; }
+
+cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if (!g_smem_attr[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(gemm_geglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        g_smem_attr[dev].store(true, std::memory_order_release);
+    }
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, a.x, a.T, a.C) || !make_map(&mw, a.w, 2 * a.F, a.C))
+        return cudaErrorInvalidValue;
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    uint16_t* table = reinterpret_cast<uint16_t*>(ws);
+    uint32_t* err = reinterpret_cast<uint32_t*>(ws + kErrOffset);
+    gelu_compact_table_kernel<<<(kCompact + 255) / 256, 256, 0, st>>>(table, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    GemmGegluParams p;
+    p.out = a.out;
+    p.s_out = a.s_out;
+    p.gate_up = a.gate_up;
+    p.s_gate_up = a.s_gate_up;
+    p.T = a.T;
+    p.C = a.C;
+    p.F = a.F;
+    p.table = table;
+    p.err = err;
+    p.num_m = (int)((a.T + BM - 1) / BM);
+    p.num_n = (int)((a.F + BNH - 1) / BNH);
+    const int64_t tiles = (int64_t)p.num_m * p.num_n;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_geglu_kernel, mx, mw, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace dtrot

@@ -16,7 +16,11 @@ References (plain torch ops on the same device and stream):
   RMSNorm  h = x + r in bf16 (bit for bit), then the norm in fp64.
 The last three must agree within 1 bf16 ulp on every element, with at most
 0.01% of the elements different (the fp64 references can still differ from
-the exactly rounded result in rounding-tie corner cases).
+the exactly rounded result in rounding-tie corner cases).  GEGLU after the
+gate_up projection is compared with the fp64 projection rounded to bf16 and
+the GEGLU reference, allowing 1% of the elements a 1-ulp difference: the
+tensor cores accumulate in fp32, so gate or up can land on the other side of
+a bf16 rounding boundary.
 
 The check costs a synchronisation and temporary tensors; it is meant for
 bring-up on a new platform or build, not for production steps.
@@ -92,7 +96,8 @@ def _is_nan(u: torch.Tensor) -> torch.Tensor:
     return ((u & 0x7F80) == 0x7F80) & ((u & 0x007F) != 0)
 
 
-def compare(name: str, got: torch.Tensor, ref: torch.Tensor, exact: bool) -> int:
+def compare(name: str, got: torch.Tensor, ref: torch.Tensor, exact: bool,
+            max_fraction: float = MAX_MISMATCH_FRACTION) -> int:
     """Raise SelfCheckError unless `got` matches `ref` (both bf16): bit for bit
     when `exact`, else within MAX_ULP on every element and in at most
     MAX_MISMATCH_FRACTION of them.  Returns the number of differing elements."""
@@ -110,7 +115,7 @@ def compare(name: str, got: torch.Tensor, ref: torch.Tensor, exact: bool) -> int
     if exact and n:
         raise SelfCheckError(f"{name}: {n} of {d.numel()} elements differ from the eager "
                              f"chain (largest difference {worst} bf16 steps)")
-    if not exact and (worst > MAX_ULP or n > MAX_MISMATCH_FRACTION * d.numel()):
+    if not exact and (worst > MAX_ULP or n > max_fraction * d.numel()):
         raise SelfCheckError(f"{name}: {n} of {d.numel()} elements differ, largest difference "
                              f"{worst} bf16 steps")
     return n

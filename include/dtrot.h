@@ -56,7 +56,8 @@ typedef enum dtrot_status {
     DTROT_ERR_LAUNCH = 6, /* the CUDA launch failed (see cudaGetLastError) */
     DTROT_ERR_DEVICE = 7, /* no current CUDA device, or it is not sm_103 */
     DTROT_ERR_VALUE = 8,  /* a scalar argument is out of range (eps) */
-    DTROT_ERR_WORKSPACE = 9 /* a workspace is smaller than required or not 16-byte aligned */
+    DTROT_ERR_WORKSPACE = 9, /* a workspace is smaller than required or not 16-byte aligned */
+    DTROT_ERR_ALIGN = 10   /* a pointer, stride or size misses an op's alignment requirement */
 } dtrot_status;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -170,6 +171,49 @@ dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate, const uint
                                 int64_t s_up, uint16_t* out, int64_t s_out, int64_t T,
                                 int64_t F, void* workspace, int64_t workspace_bytes,
                                 void* stream);
+
+/*
+ * Bytes of device workspace dtrot_gemm_gelu_and_mul needs (17408).
+ */
+int64_t dtrot_gemm_gelu_and_mul_workspace_bytes(void);
+
+/*
+ * GEGLU applied in the epilogue of the MLP's gate_up projection.   [P4] section 3
+ *
+ *   gate_up[t, n] = RN16(sum_c x[t, c] * w[n, c])      (the projection's bf16 output)
+ *   out[t, f]     = RN16(gate_up[t, F + f] * RN16(RN32(gelu(gate_up[t, f]))))
+ *
+ * i.e. gate_up_proj followed by gelu_and_mul, without gate_up ever being
+ * stored.  The sums are accumulated in fp32 on the tensor cores, in an order
+ * this library does not specify, so gate_up may differ from the rounding of
+ * the exact sum where that sum lies within the fp32 accumulation error of a
+ * bf16 rounding boundary; inputs whose partial sums are all exact in fp32
+ * give the exact result.
+ *   x         bf16, (T, C) contiguous, read only.
+ *   w         bf16, (2F, C) contiguous (an nn.Linear weight: rows [0, F) make
+ *             gate, rows [F, 2F) make up), read only.
+ *   out       bf16, (T, F), row stride s_out >= F, written; must not overlap
+ *             x, w or the workspace (DTROT_ERR_ALIAS).
+ *   gate_up   optional (NULL to skip): bf16, (T, 2F), row stride s_gate_up >=
+ *             2F, receives the rounded projection (gate columns [0, F), up
+ *             columns [F, 2F)), e.g. for a backward pass; must not overlap the
+ *             other buffers (DTROT_ERR_ALIAS).
+ *   Alignment: x, w, out (and gate_up) 16-byte aligned, C, F, s_out (and
+ *   s_gate_up) multiples of 8 (else DTROT_ERR_ALIGN).  C must be > 0 and T, 2F < 2^31 (DTROT_ERR_SHAPE).
+ *   workspace at least dtrot_gemm_gelu_and_mul_workspace_bytes() bytes,
+ *             16-byte aligned (else DTROT_ERR_WORKSPACE), owned by the caller,
+ *             contents on entry ignored: the call writes its activation table
+ *             there (bytes [0, 17152)) and an error word (bytes [17152, 17156),
+ *             zero unless a wait inside the kernel ran out of time, which
+ *             would mean the GPU stopped making progress).  Calls that may run
+ *             at the same time on the GPU must use different workspaces.
+ * Two kernels are enqueued on `stream`: the activation table, then the GEMM
+ * as its programmatic dependent.  Needs an sm_103 GPU (tcgen05 tensor cores).
+ */
+dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int64_t C, const uint16_t* w,
+                                     int64_t F, uint16_t* out, int64_t s_out, uint16_t* gate_up,
+                                     int64_t s_gate_up, void* workspace, int64_t workspace_bytes,
+                                     void* stream);
 
 /*
  * GEGLU that allocates nothing and needs no workspace.  The paper has no

@@ -35,7 +35,8 @@ def test_header_declares_the_four_ops():
     names = declared_functions()
     for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half",
                "dtrot_rope_rotate_half_qk", "dtrot_gelu_and_mul",
-               "dtrot_gelu_and_mul_workspace_bytes", "dtrot_rmsnorm_residual",
+               "dtrot_gelu_and_mul_workspace_bytes", "dtrot_gemm_gelu_and_mul",
+               "dtrot_gemm_gelu_and_mul_workspace_bytes", "dtrot_rmsnorm_residual",
                "dtrot_status_str", "dtrot_version"):
         assert op in names
 
@@ -128,6 +129,42 @@ def test_rope_qk_valid_layouts_reach_the_device_check(lib):
     assert rope_qk(q=P + 2 * 16, k=P) == _capi.ERR_DEVICE              # k heads before q heads
     assert rope_qk(k=W, sk_b=64, sk_s=16) == _capi.ERR_DEVICE          # separate buffers
     assert rope_qk(cos=0, sin=0, freqs=Q) == _capi.ERR_DEVICE          # angles
+
+
+def gemm(**kw):
+    a = dict(x=P, T=4, C=64, w=Q, F=16, out=R, so=16, gu=0, sgu=32, ws=WS, wsb=17408)
+    a.update(kw)
+    return _capi.call("dtrot_gemm_gelu_and_mul", a["x"], a["T"], a["C"], a["w"], a["F"],
+                      a["out"], a["so"], a["gu"] or None, a["sgu"], a["ws"], a["wsb"], None)
+
+
+def test_gemm_gelu_and_mul_validation(lib):
+    assert lib.dtrot_gemm_gelu_and_mul_workspace_bytes() == 17408
+    assert gemm(T=0, x=0, w=0, out=0, ws=0) == _capi.OK
+    assert gemm(F=0) == _capi.OK
+    assert gemm(C=0) == _capi.ERR_SHAPE
+    assert gemm(T=-1) == _capi.ERR_SHAPE
+    assert gemm(T=1 << 31) == _capi.ERR_SHAPE
+    assert gemm(w=0) == _capi.ERR_NULL
+    assert gemm(ws=0) == _capi.ERR_NULL
+    assert gemm(so=8) == _capi.ERR_STRIDE                  # < F
+    assert gemm(C=60) == _capi.ERR_ALIGN
+    assert gemm(F=12, so=16) == _capi.ERR_ALIGN
+    assert gemm(x=P + 8) == _capi.ERR_ALIGN
+    assert gemm(so=20) == _capi.ERR_ALIGN
+    assert gemm(wsb=17407) == _capi.ERR_WORKSPACE
+    assert gemm(ws=WS + 4) == _capi.ERR_WORKSPACE
+    assert gemm(out=P) == _capi.ERR_ALIAS                  # over x
+    assert gemm(ws=Q + 64) == _capi.ERR_ALIAS              # over w
+    assert gemm(gu=W, sgu=16) == _capi.ERR_STRIDE          # < 2F
+    assert gemm(gu=W + 8) == _capi.ERR_ALIGN
+    assert gemm(gu=R + 32) == _capi.ERR_ALIAS              # over out
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host without a GPU only")
+def test_gemm_gelu_and_mul_valid_call_reaches_device_check(lib):
+    assert gemm() == _capi.ERR_DEVICE
+    assert gemm(gu=W) == _capi.ERR_DEVICE
 
 
 def test_zero_sized_calls_are_noops(lib):
