@@ -259,9 +259,51 @@ def fused_rope_qk(dt, layer, wl, reps):
                                           "gbs": round((moved + extra) / (ms / 1e3) / 1e9, 1),
                                           "launches": 1, "reps": reps}
     del q2, k2
-    res["note"] = ("in place, one launch for q and k; 'angles' also replaces the "
-                   "rope_cos_sin_precompute launch of the step")
+    res["note"] = ("rope_qk: in place, one launch for q and k; 'angles' also replaces the "
+                   "rope_cos_sin_precompute launch of the step.  gemm_gelu_and_mul: the MLP's "
+                   "gate_up projection with GEGLU in its epilogue, gate_up never stored")
     return res
+
+
+def fused_mlp_geglu(dt, layer, wl, reps):
+    """The MLP's gate_up projection with GEGLU in its epilogue (tcgen05), on the
+    layer's pre-FFN norm output y2 (T, C) and random nn.Linear-style weights
+    (2F, C) ~ U(-1/sqrt C, 1/sqrt C); next to cuBLAS (torch.matmul) writing
+    gate_up followed by gelu_and_mul.  TFLOP/s count 2 * T * C * 2F."""
+    d = layer.d
+    x = d["y2"]
+    T, C = x.shape
+    F = wl.F
+    g = torch.Generator(device=x.device).manual_seed(wl.seed * 31 + 7)
+    w = ((torch.rand((2 * F, C), generator=g, device=x.device) * 2 - 1) / math.sqrt(C)).to(
+        torch.bfloat16)
+    out = torch.empty((T, F), dtype=torch.bfloat16, device=x.device)
+    gu = torch.empty((T, 2 * F), dtype=torch.bfloat16, device=x.device)
+    flops = 2.0 * T * C * 2 * F
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    ms_fused = timed(lambda: dt.gemm_gelu_and_mul(x, w, out=out))
+    ms_mm = timed(lambda: torch.matmul(x, w.t(), out=gu))
+    ms_act = timed(lambda: dt.gelu_and_mul(gu[:, :F], gu[:, F:], out=out))
+    del w, out, gu
+    return {"gemm_gelu_and_mul": {"ms": round(ms_fused, 4), "tflops": round(flops / ms_fused / 1e9, 1),
+                                  "launches": 2, "reps": reps,
+                                  "shape": f"x ({T}, {C}) x w ({2 * F}, {C})^T -> ({T}, {F})"},
+            "cublas_matmul_then_gelu_and_mul": {
+                "ms": round(ms_mm + ms_act, 4), "matmul_ms": round(ms_mm, 4),
+                "matmul_tflops": round(flops / ms_mm / 1e9, 1), "gelu_and_mul_ms": round(ms_act, 4)}}
 
 
 def cpu_baseline(wl, W, layer, target_s=15.0):
@@ -365,6 +407,7 @@ def native(args):
     # the next rows on the same layer: RoPE on q and k in one in-place launch,
     # with the tables or with the angles evaluated inside the kernel
     fused = fused_rope_qk(dt, layer, wl, min(K, 200))
+    fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))
 
     # end to end through host buffers: H2D inputs, the step, D2H outputs
     KE = max(1, args.e2e_steps)

@@ -43,12 +43,13 @@ constexpr int BNH = 128;            // output columns per tile (gate or up half)
 constexpr int BN = 2 * BNH;         // MMA N: gate and up columns
 constexpr int BK = 64;              // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kStages = 4;
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kGroupM = 16;
 constexpr uint32_t kATile = BM * BK * 2;   // 16 KB
 constexpr uint32_t kBTile = BN * BK * 2;   // 32 KB
 constexpr uint32_t kStageBytes = kATile + kBTile;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kAccCols = 256;   // one 128 x 256 fp32 accumulator
+constexpr uint32_t kTmemCols = 512;  // two accumulators: MMA and epilogue overlap
 
 // Compact activation table: entries for |x| in [2^-30, 8) (x > 0) and
 // [2^-30, 16) (x < 0), i.e. bf16 exponent fields 97..129 and 97..130; every
@@ -218,18 +219,39 @@ __global__ void __launch_bounds__(256) gelu_compact_table_kernel(uint16_t* __res
 
 // ---------------------------------------------------------------- the GEMM
 
+// Tile t of the grouped order: row tiles advance fastest within a group of
+// kGroupM, so the CTAs working at the same time share x and W tiles in L2.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& m0, int& f0) {
+    const int in_group = kGroupM * num_n;
+    const int first_m = (t / in_group) * kGroupM;
+    const int gm = min(num_m - first_m, kGroupM);
+    m0 = (first_m + (t % in_group) % gm) * BM;
+    f0 = ((t % in_group) / gm) * BNH;
+}
+
+// Persistent CTAs (one per SM) walk tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Roles: warp 0 lane 0 feeds the stage ring with TMA, running ahead into the
+// next tile; warp 1 lane 0 issues the MMAs into one of two accumulators in
+// tensor memory; warps 2-5 drain the other accumulator (the epilogue) while
+// the next tile's MMAs run.  Barriers: full/empty per stage, and per
+// accumulator acc_full (MMA -> epilogue, by tcgen05.commit) and acc_empty
+// (epilogue -> MMA, one arrival per epilogue warp).  A wait that runs out of
+// time sets `abort` in shared memory and every role leaves its loop.
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_geglu_kernel(const __grid_constant__ CUtensorMap tma_x,
                       const __grid_constant__ CUtensorMap tma_w, GemmGegluParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_skip;
+    __shared__ volatile uint32_t s_abort;
     // the table kernel (the prerequisite grid) has written the activation table
-    // and cleared the error word once this returns; only CTAs that start while
-    // it still runs wait here
+    // and cleared the error word once this returns
     wait_for_prerequisite_grid();
-    // a CTA that starts after an earlier one ran out of a wait does nothing
+    // a CTA that starts after an earlier launch ran out of a wait does nothing
     // (decided by one thread, so the whole CTA leaves together)
-    if (threadIdx.x == 0) s_skip = *reinterpret_cast<volatile uint32_t*>(p.err);
+    if (threadIdx.x == 0) {
+        s_skip = *reinterpret_cast<volatile uint32_t*>(p.err);
+        s_abort = 0;
+    }
     __syncthreads();
     if (s_skip != 0) return;
 
@@ -240,20 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sB = base + kStages * kATile;
     uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStages * kStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStages * kStageBytes + kTabBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStages;
-    const uint32_t accum = full0 + 16 * kStages;
+    const uint32_t acc_full0 = full0 + 16 * kStages, acc_empty0 = acc_full0 + 16;
+    const uint32_t drain = acc_empty0 + 16;  // every MMA of this CTA has completed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // tile (grouped so a wave of CTAs shares x and W tiles in L2)
-    const int pid = blockIdx.x;
-    const int in_group = kGroupM * p.num_n;
-    const int first_m = (pid / in_group) * kGroupM;
-    const int gm = min(p.num_m - first_m, kGroupM);
-    const int m_t = first_m + (pid % in_group) % gm;
-    const int n_t = (pid % in_group) / gm;
-    const int m0 = m_t * BM, f0 = n_t * BNH;
+    const int tiles = p.num_m * p.num_n;
     const int nk = (int)((p.C + BK - 1) / BK);
 
     if (threadIdx.x == 0) {
@@ -261,7 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(accum, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full0 + 8 * a, 1);
+            mbar_init(acc_empty0 + 8 * a, 4);
+        }
+        mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -280,75 +299,130 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        // TMA producer
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-            if (kb >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1u, p.err, kErrTimeoutEmpty))
+    if (warp == 0) {
+        if (lane == 0) {
+            // TMA producer; `it` counts stage uses across all tiles of this CTA
+            uint32_t it = 0;
+            for (int t = blockIdx.x; t < tiles && !s_abort; t += gridDim.x) {
+                int m0, f0;
+                tile_coords(t, p.num_m, p.num_n, m0, f0);
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (it >= (uint32_t)kStages &&
+                        !mbar_wait(empty0 + 8 * s, ph ^ 1u, p.err, kErrTimeoutEmpty)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * s;
+                    mbar_expect_tx(fb, kStageBytes);
+                    tma_load_2d(sA + s * kATile, &tma_x, kb * BK, m0, fb);
+                    tma_load_2d(sB + s * kBTile, &tma_w, kb * BK, f0, fb);
+                    tma_load_2d(sB + s * kBTile + BNH * BK * 2, &tma_w, kb * BK,
+                                (int32_t)p.F + f0, fb);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer: 4 instructions of K 16 per stage into accumulator
+            // i % 2; the stage is released when they have read it, the
+            // accumulator handed to the epilogue after the tile's last stage
+            uint32_t it = 0;
+            int i = 0;
+            for (int t = blockIdx.x; t < tiles && !s_abort; t += gridDim.x, ++i) {
+                const int acc = i & 1;
+                if (i >= 2 && !mbar_wait(acc_empty0 + 8 * acc, ((i >> 1) & 1) ^ 1, p.err,
+                                         kErrTimeoutAccum)) {
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)acc * kAccCols;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait(full0 + 8 * s, ph, p.err, kErrTimeoutFull)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a = smem_desc(sA + s * kATile);
+                    const uint64_t b = smem_desc(sB + s * kBTile);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16(d, a + 2 * k, b + 2 * k, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(empty0 + 8 * s);
+                }
+                mma_commit(acc_full0 + 8 * acc);  // after this tile's MMAs complete
+                if (s_abort) break;
+            }
+            // tensor memory is freed below only after every MMA issued here
+            // has completed (the epilogue may have stopped early on an abort)
+            mma_commit(drain);
+            mbar_wait(drain, 0, p.err, kErrTimeoutAccum);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: warp w reads accumulator lanes 32 * (w % 4) .. + 31
+        const int quarter = warp & 3;
+        int i = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const int acc = i & 1;
+            const bool ok = !s_abort && mbar_wait(acc_full0 + 8 * acc, (i >> 1) & 1, p.err,
+                                                  kErrTimeoutAccum);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, ok)) {
+                s_abort = 1;
                 break;
-            const uint32_t fb = full0 + 8 * s;
-            mbar_expect_tx(fb, kStageBytes);
-            tma_load_2d(sA + s * kATile, &tma_x, kb * BK, m0, fb);
-            tma_load_2d(sB + s * kBTile, &tma_w, kb * BK, f0, fb);
-            tma_load_2d(sB + s * kBTile + BNH * BK * 2, &tma_w, kb * BK, (int32_t)p.F + f0, fb);
-        }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer: 4 instructions of K 16 per stage, then the stage is
-        // released when they have read it
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-            if (!mbar_wait(full0 + 8 * s, ph, p.err, kErrTimeoutFull)) break;
+            }
             tc_fence_after();
-            const uint64_t a = smem_desc(sA + s * kATile);
-            const uint64_t b = smem_desc(sB + s * kBTile);
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-                mma_bf16(tmem, a + 2 * k, b + 2 * k, (kb | k) != 0 ? 1u : 0u);
-            mma_commit(empty0 + 8 * s);
-        }
-        mma_commit(accum);  // arrives once every MMA issued above has completed
-    }
-
-    const bool ok = mbar_wait(accum, 0, p.err, kErrTimeoutAccum);
-    __syncwarp();
-    tc_fence_after();
-    const int64_t row = (int64_t)m0 + warp * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+            int m0, f0;
+            tile_coords(t, p.num_m, p.num_n, m0, f0);
+            const int64_t row = (int64_t)m0 + quarter * 32 + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols;
 #pragma unroll 1
-    for (int j = 0; j < BNH / 32; ++j) {
-        uint32_t g[32], u[32];
-        tmem_ld32(taddr + 32 * j, g);
-        tmem_ld32(taddr + BNH + 32 * j, u);
-        tmem_wait_ld();
-        if (ok && row < p.T) {
-            uint32_t o[16], gb[16], ub[16];
+            for (int j = 0; j < BNH / 32; ++j) {
+                uint32_t g[32], u[32];
+                tmem_ld32(taddr + 32 * j, g);
+                tmem_ld32(taddr + BNH + 32 * j, u);
+                tmem_wait_ld();
+                if (row < p.T) {
+                    uint32_t o[16], gb[16], ub[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                gb[i] = rn16x2f(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
-                ub[i] = rn16x2f(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
-                o[i] = bmul2(ub[i], gelu_lookup2(tab, gb[i]));
-            }
-            uint16_t* dst = p.out + row * p.s_out + f0 + 32 * j;
+                    for (int q = 0; q < 16; ++q) {
+                        gb[q] = rn16x2f(__uint_as_float(g[2 * q]), __uint_as_float(g[2 * q + 1]));
+                        ub[q] = rn16x2f(__uint_as_float(u[2 * q]), __uint_as_float(u[2 * q + 1]));
+                        o[q] = bmul2(ub[q], gelu_lookup2(tab, gb[q]));
+                    }
+                    uint16_t* dst = p.out + row * p.s_out + f0 + 32 * j;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (f0 + 32 * j + 8 * q < p.F)
-                    *reinterpret_cast<uint4*>(dst + 8 * q) =
-                        make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            }
-            if (p.gate_up) {
-                uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
+                    for (int q = 0; q < 4; ++q) {
+                        if (f0 + 32 * j + 8 * q < p.F)
+                            *reinterpret_cast<uint4*>(dst + 8 * q) =
+                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
+                    if (p.gate_up) {
+                        uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (f0 + 32 * j + 8 * q < p.F) {
-                        *reinterpret_cast<uint4*>(gdst + 8 * q) =
-                            make_uint4(gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
-                        *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) =
-                            make_uint4(ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q) {
+                            if (f0 + 32 * j + 8 * q < p.F) {
+                                *reinterpret_cast<uint4*>(gdst + 8 * q) = make_uint4(
+                                    gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
+                                *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) = make_uint4(
+                                    ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
+                            }
+                        }
                     }
                 }
             }
+            // this accumulator may be overwritten once all four warps are done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                                            acc_empty0 + 8 * acc)
+                                        : "memory");
         }
     }
     tc_fence_before();
@@ -360,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kStageBytes + kTabBytes + (2 * kStages + 1) * 8 + 16;
+    1024 + (size_t)kStages * kStageBytes + kTabBytes + (2 * kStages + 5) * 8 + 16;
 
 constexpr int kMaxDev = 64;
 std::atomic<bool> g_smem_attr[kMaxDev];
@@ -439,12 +513,14 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     p.num_m = (int)((a.T + BM - 1) / BM);
     p.num_n = (int)((a.F + BNH - 1) / BNH);
     const int64_t tiles = (int64_t)p.num_m * p.num_n;
+    int64_t grid = num_sms();  // persistent: one CTA per SM (the stage ring fills its smem)
+    if (grid > tiles) grid = tiles;
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)tiles);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
