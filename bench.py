@@ -549,8 +549,10 @@ def native(args):
 # ------------------------------------------------------------------ reference arm
 
 def reference(args):
-    """The CPU oracle timed on host cores on the same workload and metric; each
-    step runs a bounded sample of the layer (a fixed slice of every op's rows)."""
+    """The CPU oracle timed on host cores on the same workload and metric.  Each
+    step runs the whole path on a sample of the layer: the first `frac` of every
+    op's rows, with `frac` calibrated so that warm-up and timed steps together
+    take about `budget_s` seconds (the step count stays the requested K)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -561,50 +563,62 @@ def reference(args):
     wl = W.WORKLOADS[args.workload]
     bts = step_bytes(wl, W)
     steps, warm = args.steps, max(3, args.warmup)
-    # rows per step sized so the whole run stays within a couple of minutes
     budget_s = 120.0
-    tok = max(1, wl.S // 4096)
-    rows_ff = max(1, wl.T_ff // 8192)
-    rows_n = max(1, wl.T_norm // 4096)
     F = wl.F
-    freqs = W.freqs_for(wl)[:tok].numpy()
-    q = oracle.bf16_bits(W.normal_bf16((wl.B, tok, wl.H, wl.D), wl.seed, 0))
-    k = oracle.bf16_bits(W.normal_bf16((wl.B, tok, wl.H, wl.D), wl.seed, 1))
-    gu = oracle.bf16_bits(W.normal_bf16((rows_ff, 2 * F), wl.seed, 2))
-    x = oracle.bf16_bits(W.normal_bf16((rows_n, wl.C), wl.seed, 4))
-    r = oracle.bf16_bits(W.normal_bf16((rows_n, wl.C), wl.seed, 5, std=2.0))
-    w = oracle.bf16_bits(W.normal_bf16((wl.C,), wl.seed, 6, mean=1.0, std=math.sqrt(0.1)))
-    sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S + 2 * bts["rope_rotate_half_q"] * tok / wl.S
-               + bts["gelu_and_mul"] * rows_ff / wl.T_ff + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
 
-    def one():
-        c, s = oracle.rope_cos_sin(freqs)
-        oracle.rope_rotate_half(q, c, s)
-        oracle.rope_rotate_half(k, c, s)
-        oracle.gelu_and_mul(gu[:, :F], gu[:, F:])
-        oracle.rmsnorm_residual(x, r, w, 1e-6)
-        oracle.rmsnorm_residual(x, r, w, 1e-6)
+    def make(frac):
+        tok = max(1, int(wl.S * frac))
+        rows_ff = max(1, int(wl.T_ff * frac))
+        rows_n = max(1, int(wl.T_norm * frac))
+        data = {
+            "freqs": W.freqs_for(wl)[:tok].numpy(),
+            "q": oracle.bf16_bits(W.normal_bf16((wl.B, tok, wl.H, wl.D), wl.seed, 0)),
+            "k": oracle.bf16_bits(W.normal_bf16((wl.B, tok, wl.H, wl.D), wl.seed, 1)),
+            "gu": oracle.bf16_bits(W.normal_bf16((rows_ff, 2 * F), wl.seed, 2)),
+            "x": oracle.bf16_bits(W.normal_bf16((rows_n, wl.C), wl.seed, 4)),
+            "r": oracle.bf16_bits(W.normal_bf16((rows_n, wl.C), wl.seed, 5, std=2.0)),
+            "w": oracle.bf16_bits(W.normal_bf16((wl.C,), wl.seed, 6, mean=1.0,
+                                                std=math.sqrt(0.1))),
+        }
+        sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S
+                   + 2 * bts["rope_rotate_half_q"] * tok / wl.S
+                   + bts["gelu_and_mul"] * rows_ff / wl.T_ff
+                   + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
+        return data, sampled, (tok, rows_ff, rows_n)
 
+    def one(d):
+        c, s_ = oracle.rope_cos_sin(d["freqs"])
+        oracle.rope_rotate_half(d["q"], c, s_)
+        oracle.rope_rotate_half(d["k"], c, s_)
+        oracle.gelu_and_mul(d["gu"][:, :F], d["gu"][:, F:])
+        oracle.rmsnorm_residual(d["x"], d["r"], d["w"], 1e-6)
+        oracle.rmsnorm_residual(d["x"], d["r"], d["w"], 1e-6)
+
+    # calibration on 1/256 of the layer, then the sample that fills the budget
+    cal_frac = 1.0 / 256
+    data, sampled, _ = make(cal_frac)
+    one(data)
     t0 = time.perf_counter()
-    one()
-    per = time.perf_counter() - t0
-    if per * (steps + warm) > budget_s:
-        steps = max(1, int(budget_s / per) - warm)
+    one(data)
+    per_frac = (time.perf_counter() - t0) / cal_frac
+    frac = min(1.0, max(1.0 / 4096, budget_s / (steps + warm) / per_frac))
+    data, sampled, (tok, rows_ff, rows_n) = make(frac)
     for _ in range(warm):
-        one()
+        one(data)
     t0 = time.perf_counter()
     for _ in range(steps):
-        one()
+        one(data)
     el = time.perf_counter() - t0
     value = sampled * steps / el / 1e9
-    sample = (f"{wl.name} layer, per step: {tok} tokens of tables and q/k RoPE, {rows_ff} GEGLU "
-              f"rows, {rows_n} rows for each RMSNorm ({sampled / 1e6:.2f} MB algorithmic)")
+    sample = (f"{wl.name} layer, per step: {tok} of {wl.S} tokens of tables and q/k RoPE, "
+              f"{rows_ff} of {wl.T_ff} GEGLU rows, {rows_n} of {wl.T_norm} rows for each "
+              f"RMSNorm ({sampled / 1e6:.1f} MB algorithmic)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * el / steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 (emulated in fp64)", "data": "synthetic",
-        "config": {"workload": f"{wl.name} DiT layer (bounded sample per step)",
+        "config": {"workload": f"{wl.name} DiT layer (a sample of every op's rows per step)",
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
