@@ -524,6 +524,10 @@ def native(args):
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "mtokens_per_s_per_layer": round(tokens / (layer_ms / 1e3) / 1e6, 3),
+        "mtokens_per_s_per_layer_with_next_rows": round(
+            tokens / ((fused["rope_qk_inplace_angles"]["ms"] + kern_ms["gelu_and_mul"]
+                       + kern_ms["rmsnorm_residual_attn"] + kern_ms["rmsnorm_residual_ffn"])
+                      / 1e3) / 1e6, 3),
         "kernels": {op: {"ms": round(kern_ms[op], 5), "bytes": bts[op],
                          "gbs": round(bts[op] / (kern_ms[op] / 1e3) / 1e9, 1)} for op in OPS},
         "roofline": {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),

@@ -252,9 +252,15 @@ def gemm_gelu_and_mul(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None
                 so, gp or None, sgu, workspace.data_ptr(),
                 workspace.numel() * workspace.element_size(), st)
     if key:
-        gu = (x.double() @ w.double().t()).float().to(torch.bfloat16)
-        _sc.compare("gemm_gelu_and_mul", out, _sc.ref_geglu(gu[:, :F], gu[:, F:]), exact=False,
-                    max_fraction=1e-2)
+        def rerun(rows):
+            o = torch.empty((rows, F), dtype=torch.bfloat16, device=x.device)
+            g = torch.empty((rows, 2 * F), dtype=torch.bfloat16, device=x.device)
+            _capi.check("dtrot_gemm_gelu_and_mul", x.data_ptr(), rows, C, w.data_ptr(), F,
+                        o.data_ptr(), F, g.data_ptr(), 2 * F, workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), st)
+            return o, g
+
+        _sc.check_gemm_geglu(x, w, out, rerun)
     return out
 
 

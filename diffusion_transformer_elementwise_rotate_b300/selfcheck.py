@@ -18,9 +18,13 @@ The last three must agree within 1 bf16 ulp on every element, with at most
 0.01% of the elements different (the fp64 references can still differ from
 the exactly rounded result in rounding-tie corner cases).  GEGLU after the
 gate_up projection is compared with the fp64 projection rounded to bf16 and
-the GEGLU reference, allowing 1% of the elements a 1-ulp difference: the
-tensor cores accumulate in fp32, so gate or up can land on the other side of
-a bf16 rounding boundary.
+the projection is checked on its first 256 rows, which the kernel runs again
+with the rounded gate_up stored: the rerun must give the same output bits,
+the output must be the GEGLU reference of the stored gate and up (the
+tolerance above), and every stored gate and up must lie within the bf16
+rounding of the fp64 projection widened by the fp32 accumulation bound
+(C + 1) * 2^-23 * sum|x w| (the tensor cores sum in fp32 in their own order,
+so near-cancelling sums can move by several bf16 steps).
 
 The check costs a synchronisation and temporary tensors; it is meant for
 bring-up on a new platform or build, not for production steps.
@@ -154,3 +158,25 @@ def ref_rmsnorm(x: torch.Tensor, r: torch.Tensor, w: torch.Tensor, eps: float):
     eps32 = float(torch.tensor(eps, dtype=torch.float32))  # the kernels take eps as fp32
     inv = torch.rsqrt(hd.pow(2).mean(dim=-1, keepdim=True) + eps32)
     return h, (hd * inv * w.double()).float().to(torch.bfloat16)
+
+
+def check_gemm_geglu(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor, rerun) -> None:
+    """GEGLU after the gate_up projection, on a sample of rows.  `rerun(rows)`
+    runs the kernel on x[:rows] and returns (out, gate_up) for them."""
+    T, C = x.shape
+    F = w.shape[0] // 2
+    rows = min(T, 256)
+    out_s, gu = rerun(rows)
+    compare("gemm_gelu_and_mul rerun", out_s, out[:rows], exact=True)
+    compare("gemm_gelu_and_mul epilogue", out[:rows], ref_geglu(gu[:, :F], gu[:, F:]), exact=False)
+    xd, wd = x[:rows].double(), w.double()
+    dot = xd @ wd.t()
+    mag = xd.abs() @ wd.abs().t()
+    eps = (C + 1) * 2.0 ** -23
+    lo = _ordered((dot - eps * mag).float().to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF)
+    hi = _ordered((dot + eps * mag).float().to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF)
+    k = _ordered(gu.contiguous().view(torch.int16).to(torch.int32) & 0xFFFF)
+    bad = int(((k < lo - 1) | (k > hi + 1)).sum().item())
+    if bad:
+        raise SelfCheckError(f"gemm_gelu_and_mul: {bad} gate/up values outside the fp32 "
+                             "accumulation bounds of the projection")

@@ -449,3 +449,58 @@ def test_work_is_enqueued_on_the_current_stream():
     s.synchronize()
     cos_b, sin_b = oracle.rope_cos_sin(W.freqs_for(wl).numpy())
     assert_bitexact(bits(out), oracle.rope_rotate_half(bits(x), cos_b, sin_b), "side stream")
+
+
+# ---------------------------------------------------------------- beyond 2^31 elements
+
+def _device_normal(shape, seed, std=1.0):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    return (torch.randn(shape, generator=g, device=DEV) * std).to(torch.bfloat16)
+
+
+def _sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, n - 1], rng.choice(n, k, replace=False)]))
+
+
+def test_geglu_beyond_2_31_elements():
+    T, F = 163841, 13200                       # T * F > 2^31, F % 8 == 0
+    gu = _device_normal((T, 2 * F), 1)
+    out = dt.gelu_and_mul_fused(gu)
+    torch.cuda.synchronize()
+    rows = _sample_rows(T, 16, 1)
+    r = torch.from_numpy(rows).to(DEV)
+    g = bits(gu[r])
+    assert_bitexact(bits(out[r]), oracle.gelu_and_mul(g[:, :F], g[:, F:]), "2^31+ GEGLU")
+    del gu, out
+
+
+def test_rmsnorm_beyond_2_31_elements():
+    T, C = 419431, 5120                        # T * C > 2^31
+    x = _device_normal((T, C), 2)
+    r = _device_normal((T, C), 3, std=2.0)
+    w = _device_normal((C,), 4, std=0.316) + 1.0
+    w = w.to(torch.bfloat16)
+    rows = _sample_rows(T, 16, 2)
+    idx = torch.from_numpy(rows).to(DEV)
+    x0, r0 = bits(x[idx]), bits(r[idx])
+    y = dt.rmsnorm_residual(x, r, w, EPS)
+    torch.cuda.synchronize()
+    h_exp, y_exp = oracle.rmsnorm_residual(x0, r0, bits(w), EPS)
+    assert_bitexact(bits(r[idx]), h_exp, "2^31+ residual")
+    assert_within_tolerance(bits(y[idx]), y_exp, "2^31+ rmsnorm")
+    del x, r, y
+
+
+def test_rope_beyond_2_31_elements():
+    B, S, H, D = 1, 32760, 512, 128            # 2.15e9 elements
+    x = _device_normal((B, S, H, D), 5)
+    freqs = W.freqs_1d(S, B, D)
+    c, s = dt.rope_cos_sin_precompute(to_dev(freqs))
+    out = dt.rope_rotate_half(x, c, s)
+    torch.cuda.synchronize()
+    toks = _sample_rows(S, 16, 3)
+    t = torch.from_numpy(toks).to(DEV)
+    cb, sb = bits(c[t]), bits(s[t])
+    assert_bitexact(bits(out[:, t]), oracle.rope_rotate_half(bits(x[:, t]), cb, sb), "2^31+ rope")
+    del x, out

@@ -113,9 +113,12 @@ def test_every_op_passes_the_check_on_the_gpu():
             n = len(sc.checked())
             dt.rmsnorm_residual(x, r, w, 1e-6)                 # same key: not checked again
             assert len(sc.checked()) == n
+            xm = W.normal_bf16((300, 512), 41, 0).cuda()
+            wm = (torch.rand((2 * 256, 512), device="cuda") * 2 - 1).mul(512 ** -0.5)
+            dt.gemm_gelu_and_mul(xm, wm.to(torch.bfloat16))
         ops = {k[0] for k in sc.checked()}
         assert ops == {"rope_cos_sin_precompute", "rope_rotate_half", "rope_rotate_half_qk",
-                       "gelu_and_mul", "rmsnorm_residual"}
+                       "gelu_and_mul", "rmsnorm_residual", "gemm_gelu_and_mul"}
     finally:
         sc.disable()
         sc.reset()
