@@ -7,7 +7,7 @@ pointers, sizes and strides; `_capi` is the raw ctypes binding.
 """
 from . import selfcheck  # noqa: F401
 from ._capi import DtrotError, DtrotUnavailable, load  # noqa: F401
-from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_workspace,  # noqa: F401
+from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_table, gelu_workspace,  # noqa: F401
                   gemm_gelu_and_mul,
                   rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half,
                   rope_rotate_half_qk_)

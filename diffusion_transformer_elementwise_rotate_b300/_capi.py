@@ -44,6 +44,9 @@ SIGNATURES = {
     "dtrot_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
     "dtrot_gelu_and_mul": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p, _i64,
                                           _p]),
+    "dtrot_gelu_table_build": (ctypes.c_int, [_p, _i64, _p]),
+    "dtrot_gelu_and_mul_with_table": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64,
+                                                     _p, _i64, _p]),
     "dtrot_gemm_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
     "dtrot_gemm_gelu_and_mul": (ctypes.c_int, [_p, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
                                                _p, _i64, _p]),

@@ -9,7 +9,8 @@ runs in libdtrot's sm_103a kernels.
   rope_rotate_half(x, cos, sin, out=None) -> out         ERNIE-Image page, section 2
   rope_rotate_half_qk_(q, k, cos=None, sin=None, freqs=None)   q and k in place, one launch;
                                          tables, or angles evaluated in the kernel
-  gelu_and_mul(gate, up, out=None, workspace=None) -> out     ERNIE-Image page, section 3
+  gelu_and_mul(gate, up, out=None, workspace=None, table=None) -> out   ERNIE-Image page, section 3
+  gelu_table(device)                      -> the activation table, built once per device
   gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
   gemm_gelu_and_mul(x, w, out=None, workspace=None) -> out   GEGLU in the epilogue of the
                                          gate_up projection x w^T (tcgen05 tensor cores)
@@ -173,11 +174,40 @@ def gelu_workspace(device: torch.device, stream: int) -> torch.Tensor:
     return ws
 
 
+_tables: dict = {}
+
+
+def gelu_table(device) -> torch.Tensor:
+    """The activation table of `device`, built once (on the current stream,
+    with an event that later calls on other streams wait for) and kept."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    with _ws_lock:
+        entry = _tables.get(idx)
+        if entry is None:
+            n = int(_capi.load().dtrot_gelu_and_mul_workspace_bytes())
+            dev = torch.device("cuda", idx)
+            tab = torch.empty(n, dtype=torch.uint8, device=dev)
+            st = torch.cuda.current_stream(dev)
+            _capi.check("dtrot_gelu_table_build", tab.data_ptr(), n, st.cuda_stream)
+            ready = torch.cuda.Event()
+            ready.record(st)
+            entry = (tab, ready)
+            _tables[idx] = entry
+    tab, ready = entry
+    torch.cuda.current_stream(tab.device).wait_event(ready)
+    return tab
+
+
 def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor, out: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+                 workspace: torch.Tensor | None = None,
+                 table: torch.Tensor | None = None) -> torch.Tensor:
     """gate, up bf16 (T, F) (row strides allowed) -> out bf16 (T, F).
     `workspace` (a CUDA buffer of dtrot_gelu_and_mul_workspace_bytes() bytes)
-    defaults to a buffer cached per device and stream."""
+    defaults to a buffer cached per device and stream; the call builds the
+    activation table there.  With `table` (from gelu_table()), the table is
+    not rebuilt."""
     _need(gate, "gate", torch.bfloat16)
     _need(up, "up", torch.bfloat16)
     if gate.shape != up.shape:
@@ -191,6 +221,17 @@ def gelu_and_mul(gate: torch.Tensor, up: torch.Tensor, out: torch.Tensor | None 
         raise ValueError("out must be (T, F)")
     so = _rows(out, "out")
     st = _stream(gate)
+    if table is not None:
+        if not table.is_cuda:
+            raise ValueError("table must be a CUDA tensor")
+        key = _sc.want("gelu_and_mul", gate, up)
+        ref = _sc.ref_geglu(gate, up) if key else None
+        _capi.check("dtrot_gelu_and_mul_with_table", gate.data_ptr(), sg, up.data_ptr(), su,
+                    out.data_ptr(), so, T, F, table.data_ptr(),
+                    table.numel() * table.element_size(), st)
+        if key:
+            _sc.compare("gelu_and_mul", out, ref, exact=False)
+        return out
     if workspace is None:
         workspace = gelu_workspace(gate.device, st)
     elif not workspace.is_cuda:

@@ -343,17 +343,9 @@ DTROT_API dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_
     return launch_status(launch_rope_qk(p, (cudaStream_t)stream));
 }
 
-DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
-                                          const uint16_t* up, int64_t s_up, uint16_t* out,
-                                          int64_t s_out, int64_t T, int64_t F, void* workspace,
-                                          int64_t workspace_bytes, void* stream) {
-    if (T < 0 || F < 0) return DTROT_ERR_SHAPE;
-    int64_t n;
-    if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
-    if (n == 0) return DTROT_OK;
-    if (!gate || !up || !out || !workspace) return DTROT_ERR_NULL;
-    if (workspace_bytes < (int64_t)gelu_table_bytes() || (uintptr_t)workspace % 16)
-        return DTROT_ERR_WORKSPACE;
+// Strides, spans and overlaps of a GEGLU call's gate, up and out; fills p.
+static dtrot_status geglu_views(const uint16_t* gate, int64_t s_gate, const uint16_t* up, int64_t s_up,
+                         uint16_t* out, int64_t s_out, int64_t T, int64_t F, GegluParams* p) {
     if (T > 1 && (s_gate < F || s_up < F || s_out < F)) return DTROT_ERR_STRIDE;
     if (s_gate < 0 || s_up < 0 || s_out < 0) return DTROT_ERR_STRIDE;
     const int64_t sg = T > 1 ? s_gate : F, su = T > 1 ? s_up : F, so = T > 1 ? s_out : F;
@@ -367,25 +359,72 @@ DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
     const bool in_place = (out == gate) && (so == sg);
     if (!in_place && !views2d_disjoint(out, so, gate, sg, T, F)) return DTROT_ERR_ALIAS;
     if (!views2d_disjoint(out, so, up, su, T, F)) return DTROT_ERR_ALIAS;
+    p->gate = gate;
+    p->up = up;
+    p->out = out;
+    p->s_gate = sg;
+    p->s_up = su;
+    p->s_out = so;
+    p->T = T;
+    p->F = F;
+    return DTROT_OK;
+}
+
+DTROT_API dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate,
+                                          const uint16_t* up, int64_t s_up, uint16_t* out,
+                                          int64_t s_out, int64_t T, int64_t F, void* workspace,
+                                          int64_t workspace_bytes, void* stream) {
+    if (T < 0 || F < 0) return DTROT_ERR_SHAPE;
+    int64_t n;
+    if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!gate || !up || !out || !workspace) return DTROT_ERR_NULL;
+    if (workspace_bytes < (int64_t)gelu_table_bytes() || (uintptr_t)workspace % 16)
+        return DTROT_ERR_WORKSPACE;
+    GegluParams p;
+    const dtrot_status v = geglu_views(gate, s_gate, up, s_up, out, s_out, T, F, &p);
+    if (v != DTROT_OK) return v;
     {
         // the workspace is written: it must not overlap gate, up or out
         const int64_t wb = (int64_t)gelu_table_bytes();
-        if (!range_disjoint(workspace, wb, gate, sg, T, F) ||
-            !range_disjoint(workspace, wb, up, su, T, F) ||
-            !range_disjoint(workspace, wb, out, so, T, F))
+        if (!range_disjoint(workspace, wb, gate, p.s_gate, T, F) ||
+            !range_disjoint(workspace, wb, up, p.s_up, T, F) ||
+            !range_disjoint(workspace, wb, out, p.s_out, T, F))
             return DTROT_ERR_ALIAS;
     }
     if (!device_ok()) return DTROT_ERR_DEVICE;
-    GegluParams p;
-    p.gate = gate;
-    p.up = up;
-    p.out = out;
-    p.s_gate = sg;
-    p.s_up = su;
-    p.s_out = so;
-    p.T = T;
-    p.F = F;
     return launch_status(launch_gelu_and_mul(p, (uint16_t*)workspace, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_gelu_table_build(void* table, int64_t table_bytes, void* stream) {
+    if (!table) return DTROT_ERR_NULL;
+    if (table_bytes < (int64_t)gelu_table_bytes() || (uintptr_t)table % 16)
+        return DTROT_ERR_WORKSPACE;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    return launch_status(launch_gelu_table((uint16_t*)table, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_gelu_and_mul_with_table(const uint16_t* gate, int64_t s_gate,
+                                                     const uint16_t* up, int64_t s_up,
+                                                     uint16_t* out, int64_t s_out, int64_t T,
+                                                     int64_t F, const void* table,
+                                                     int64_t table_bytes, void* stream) {
+    if (T < 0 || F < 0) return DTROT_ERR_SHAPE;
+    int64_t n;
+    if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
+    if (n == 0) return DTROT_OK;
+    if (!gate || !up || !out || !table) return DTROT_ERR_NULL;
+    if (table_bytes < (int64_t)gelu_table_bytes() || (uintptr_t)table % 16)
+        return DTROT_ERR_WORKSPACE;
+    GegluParams p;
+    const dtrot_status v = geglu_views(gate, s_gate, up, s_up, out, s_out, T, F, &p);
+    if (v != DTROT_OK) return v;
+    // the table is only read: it must not overlap out, which is written
+    if (!range_disjoint(table, (int64_t)gelu_table_bytes(), out, p.s_out, T, F))
+        return DTROT_ERR_ALIAS;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    return launch_status(
+        launch_gelu_stream(p, (const uint16_t*)table, false, (cudaStream_t)stream));
 }
 
 // GEGLU for callers that cannot allocate device memory: the same computation

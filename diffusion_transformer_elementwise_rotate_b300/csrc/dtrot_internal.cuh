@@ -196,6 +196,11 @@ size_t gemm_geglu_workspace_bytes();
 cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st);
 size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);
+cudaError_t launch_gelu_table(uint16_t* table, cudaStream_t st);
+// The streaming kernel alone, on a table already built (after_table: launched
+// right behind the table kernel, as its programmatic dependent).
+cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table, bool after_table,
+                               cudaStream_t st);
 // Device address and size of the library-owned activation table of the
 // current device (looked up on the first call per device).
 cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity);

@@ -159,7 +159,13 @@ cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity) {
     return cudaSuccess;
 }
 
-cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st) {
+cudaError_t launch_gelu_table(uint16_t* table, cudaStream_t st) {
+    gelu_table_kernel<<<kTable / 256, 256, 0, st>>>(table);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table, bool after_table,
+                               cudaStream_t st) {
     const size_t smem = kTable * sizeof(uint16_t);
     const bool vec = (p.F % 8 == 0) && (p.s_gate % 8 == 0) && (p.s_up % 8 == 0) &&
                      (p.s_out % 8 == 0) && aligned(p.gate, 16) && aligned(p.up, 16) &&
@@ -184,11 +190,9 @@ cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStrea
         if (e != cudaSuccess) return e;
         g_attr[dev][which].store(true, std::memory_order_release);
     }
-    gelu_table_kernel<<<kTable / 256, 256, 0, st>>>(table);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // the streaming kernel may start before the table kernel completes; it
-    // waits for it with griddepcontrol.wait before touching the table
+    // right after the table kernel, the streaming kernel is its programmatic
+    // dependent: it may start before the table kernel completes and waits for
+    // it with griddepcontrol.wait before touching the table (a no-op otherwise)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -198,14 +202,19 @@ cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStrea
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const uint16_t* gtab = table;
+    cfg.numAttrs = after_table ? 1 : 0;
     if (vec)
-        e = cudaLaunchKernelEx(&cfg, geglu_vec_kernel<4>, p, gtab);
+        e = cudaLaunchKernelEx(&cfg, geglu_vec_kernel<4>, p, table);
     else
-        e = cudaLaunchKernelEx(&cfg, geglu_scalar_kernel, p, gtab);
+        e = cudaLaunchKernelEx(&cfg, geglu_scalar_kernel, p, table);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st) {
+    cudaError_t e = launch_gelu_table(table, st);
+    if (e != cudaSuccess) return e;
+    return launch_gelu_stream(p, table, true, st);
 }
 
 }  // namespace dtrot

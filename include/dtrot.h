@@ -173,6 +173,32 @@ dtrot_status dtrot_gelu_and_mul(const uint16_t* gate, int64_t s_gate, const uint
                                 void* stream);
 
 /*
+ * GEGLU with an activation table built once and kept.        [P4] sections 1, 3
+ *
+ * The activation table of dtrot_gelu_and_mul depends on nothing but the
+ * function (one entry per bf16 gate value), so a caller that runs GEGLU many
+ * times (every layer of every step) can build it once, as the ERNIE-Image page
+ * hoists the cos/sin rows out of the per-layer path, and skip the table launch
+ * on every call.
+ *
+ * dtrot_gelu_table_build fills `table` (at least
+ * dtrot_gelu_and_mul_workspace_bytes() bytes, 16-byte aligned, else
+ * DTROT_ERR_WORKSPACE) with the table, one kernel on `stream`.
+ *
+ * dtrot_gelu_and_mul_with_table computes exactly what dtrot_gelu_and_mul
+ * computes, with the same arguments, layouts and errors, except that `table`
+ * must hold a table written by dtrot_gelu_table_build and is only read: work
+ * on other streams must be ordered after the build, the caller must not
+ * modify the table, and out must not overlap it (DTROT_ERR_ALIAS).
+ */
+dtrot_status dtrot_gelu_table_build(void* table, int64_t table_bytes, void* stream);
+dtrot_status dtrot_gelu_and_mul_with_table(const uint16_t* gate, int64_t s_gate,
+                                           const uint16_t* up, int64_t s_up, uint16_t* out,
+                                           int64_t s_out, int64_t T, int64_t F,
+                                           const void* table, int64_t table_bytes,
+                                           void* stream);
+
+/*
  * Bytes of device workspace dtrot_gemm_gelu_and_mul needs (17408).
  */
 int64_t dtrot_gemm_gelu_and_mul_workspace_bytes(void);

@@ -35,7 +35,8 @@ def test_header_declares_the_four_ops():
     names = declared_functions()
     for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half",
                "dtrot_rope_rotate_half_qk", "dtrot_gelu_and_mul",
-               "dtrot_gelu_and_mul_workspace_bytes", "dtrot_gemm_gelu_and_mul",
+               "dtrot_gelu_and_mul_workspace_bytes", "dtrot_gelu_table_build",
+               "dtrot_gelu_and_mul_with_table", "dtrot_gemm_gelu_and_mul",
                "dtrot_gemm_gelu_and_mul_workspace_bytes", "dtrot_rmsnorm_residual",
                "dtrot_status_str", "dtrot_version"):
         assert op in names
@@ -245,6 +246,33 @@ def test_gelu_workspace(lib):
     # starts in that gap but runs into row 1 of gate (element sg)
     assert geglu(sg=sg, su=sg, up=P + 16, ws=P + 2 * (sg - 65536 + 8)) == _capi.ERR_ALIAS
     assert geglu(sg=sg, su=sg, up=P + 16, ws=P + 2 * sg) == _capi.ERR_ALIAS
+
+
+def geglu_tab(**kw):
+    a = dict(gate=P, sg=16, up=P + 16, su=16, out=W, so=8, T=4, F=8, tab=WS, tb=WS_BYTES)
+    a.update(kw)
+    return _capi.call("dtrot_gelu_and_mul_with_table", a["gate"], a["sg"], a["up"], a["su"],
+                      a["out"], a["so"], a["T"], a["F"], a["tab"], a["tb"], None)
+
+
+def test_prebuilt_gelu_table_validation(lib):
+    assert _capi.call("dtrot_gelu_table_build", None, WS_BYTES, None) == _capi.ERR_NULL
+    assert _capi.call("dtrot_gelu_table_build", WS, WS_BYTES - 2, None) == _capi.ERR_WORKSPACE
+    assert _capi.call("dtrot_gelu_table_build", WS + 8, WS_BYTES, None) == _capi.ERR_WORKSPACE
+    assert geglu_tab(T=0, gate=0, up=0, out=0, tab=0) == _capi.OK
+    assert geglu_tab(tab=0) == _capi.ERR_NULL
+    assert geglu_tab(tb=100) == _capi.ERR_WORKSPACE
+    assert geglu_tab(tab=WS + 4) == _capi.ERR_WORKSPACE
+    assert geglu_tab(sg=4) == _capi.ERR_STRIDE
+    assert geglu_tab(out=P + 16, so=16) == _capi.ERR_ALIAS          # out over up
+    assert geglu_tab(tab=W - 64) == _capi.ERR_ALIAS                 # table runs into out
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host without a GPU only")
+def test_prebuilt_gelu_table_valid_calls_reach_device_check(lib):
+    assert _capi.call("dtrot_gelu_table_build", WS, WS_BYTES, None) == _capi.ERR_DEVICE
+    assert geglu_tab() == _capi.ERR_DEVICE
+    assert geglu_tab(tab=P) == _capi.ERR_DEVICE                     # table over gate: both read
 
 
 def test_eps(lib):

@@ -338,6 +338,26 @@ def test_geglu_caller_workspace_is_rebuilt_every_call():
         dt.gelu_and_mul(to_dev(from_u16(gate)), to_dev(from_u16(up)), workspace=small)
 
 
+def test_geglu_prebuilt_table_every_gate_value_and_video_rows():
+    tab = dt.gelu_table("cuda")
+    gate = np.arange(1 << 16, dtype=np.uint16).reshape(128, 512)
+    up = bits(W.normal_bf16((128, 512), 13, 3, std=2.0))
+    got = dt.gelu_and_mul(to_dev(from_u16(gate)), to_dev(from_u16(up)), table=tab)
+    assert_bitexact(bits(got), oracle.gelu_and_mul(gate, up), "prebuilt table, every gate")
+    wl = W.WORKLOADS["video"]
+    gu = to_dev(W.geglu_inputs(wl))
+    F = wl.F
+    out = dt.gelu_and_mul(gu[:, :F], gu[:, F:], table=tab)
+    ref = dt.gelu_and_mul(gu[:, :F], gu[:, F:])              # the table rebuilt in the call
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    rows = np.unique(np.concatenate([[0, wl.T_ff - 1],
+                                     np.random.default_rng(6).choice(wl.T_ff, 64, replace=False)]))
+    r = torch.from_numpy(rows).to(DEV)
+    g = bits(gu[r])
+    assert_bitexact(bits(out[r]), oracle.gelu_and_mul(g[:, :F], g[:, F:]), "prebuilt, video rows")
+
+
 def test_geglu_empty():
     z = torch.empty((0, 16), dtype=torch.bfloat16, device=DEV)
     assert dt.gelu_and_mul(z, z).shape == (0, 16)
