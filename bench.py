@@ -436,11 +436,29 @@ def cpu_baseline(wl, W, layer, target_s=15.0):
                    + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
         return dt_s, sampled, (tok, rows_ff, rows_n)
 
+    def fill(frac, target):
+        """Rescale the sample until one run takes at least half of `target`."""
+        t, sampled, rows = run(frac)
+        while t < 0.5 * target and frac < 1.0:
+            frac = min(1.0, frac * target / max(t, 1e-3))
+            t, sampled, rows = run(frac)
+        return t, sampled, rows
+
     run(1.0 / 2048)  # warm-up (thread pool start-up)
-    t, _, _ = run(1.0 / 256)  # calibration
-    frac = min(1.0, (1.0 / 256) * target_s / max(t, 1e-3))
-    t, sampled, (tok, rf, rn) = run(frac)
-    return {"value": round(sampled / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+    t, sampled, (tok, rf, rn) = fill(1.0 / 256, target_s)
+    # one core, on a sample a few seconds long (rows are independent, so the
+    # rate carries over to the whole layer)
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t1, sampled1, (tok1, rf1, rn1) = fill(1.0 / 2048, target_s / 3)
+    finally:
+        oracle.set_num_threads(cores)
+    single = {"value": round(sampled1 / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+              "sample": (f"first {tok1} tokens, {rf1} GEGLU rows, {rn1} rows per RMSNorm; "
+                         f"{sampled1 / 1e9:.3f} GB in {t1:.2f} s")}
+    return {"value": round(sampled / t / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "single_core": single,
             "kind": "oracle",
             "sample": (f"{wl.name} layer: first {tok} of {wl.S} tokens for the tables and q/k "
                        f"RoPE, first {rf} of {wl.T_ff} GEGLU rows, first {rn} of {wl.T_norm} "

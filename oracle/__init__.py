@@ -76,6 +76,8 @@ def lib():
         L.dto_rmsnorm_residual_f64.restype = None
         L.dto_gate_up_bf16.argtypes = [_p, _i64, _i64, _p, _i64, ctypes.c_double, _p, _p, _p]
         L.dto_gate_up_bf16.restype = None
+        L.dto_set_num_threads.argtypes = [ctypes.c_int]
+        L.dto_set_num_threads.restype = None
         L.dto_num_threads.argtypes = []
         L.dto_num_threads.restype = ctypes.c_int
         if not L.dto_fp_env_ok():
@@ -86,6 +88,11 @@ def lib():
 
 def num_threads() -> int:
     return int(lib().dto_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the row loops use from now on (results do not depend on it)."""
+    lib().dto_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- helpers

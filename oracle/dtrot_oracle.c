@@ -313,6 +313,9 @@ EXPORT void dto_gate_up_bf16(const uint16_t* x, int64_t T, int64_t C, const uint
 #ifdef _OPENMP
 #include <omp.h>
 EXPORT int dto_num_threads(void) { return omp_get_max_threads(); }
+/* Threads for the following calls (the results do not depend on it). */
+EXPORT void dto_set_num_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 #else
 EXPORT int dto_num_threads(void) { return 1; }
+EXPORT void dto_set_num_threads(int n) { (void)n; }
 #endif

@@ -524,3 +524,87 @@ def test_rope_beyond_2_31_elements():
     cb, sb = bits(c[t]), bits(s[t])
     assert_bitexact(bits(out[:, t]), oracle.rope_rotate_half(bits(x[:, t]), cb, sb), "2^31+ rope")
     del x, out
+
+
+# ---------------------------------------------------------------- row subsets, canaries
+
+def test_geglu_and_rope_row_subsets_equal_the_full_run():
+    wl = W.WORKLOADS["image"]
+    gu = to_dev(W.geglu_inputs(wl))
+    full = dt.gelu_and_mul_fused(gu)
+    for a, b in [(0, 1), (17, 530), (4000, 4096)]:
+        part = dt.gelu_and_mul_fused(gu[a:b].contiguous())
+        assert torch.equal(part.view(torch.int16), full[a:b].view(torch.int16)), (a, b)
+    x = to_dev(W.rope_inputs(wl, "q"))
+    c, s = dt.rope_cos_sin_precompute(to_dev(W.freqs_for(wl)))
+    full = dt.rope_rotate_half(x, c, s)
+    for a, b in [(0, 1), (333, 1000), (4095, 4096)]:
+        part = dt.rope_rotate_half(x[:, a:b], c[a:b].contiguous(), s[a:b].contiguous())
+        assert torch.equal(part.view(torch.int16), full[:, a:b].view(torch.int16)), (a, b)
+
+
+CANARY = 0x7E7E  # a bf16 pattern no op writes here by chance
+
+
+def _canvas(shape, pad):
+    """A buffer with `pad` canary columns on each side of the last dimension and
+    one canary row before and after; returns (buffer, the inner view)."""
+    *lead, n = shape
+    buf = torch.full((*lead[:-1], lead[-1] + 2, n + 2 * pad) if lead else (n + 2 * pad,), 0,
+                     dtype=torch.int16, device=DEV)
+    buf.fill_(CANARY)
+    buf = buf.view(torch.bfloat16)
+    inner = buf[..., 1:-1, pad:pad + n] if lead else buf[pad:pad + n]
+    return buf, inner
+
+
+def _canary_intact(buf, inner):
+    b = buf.view(torch.int16).clone()
+    mask = torch.ones_like(b, dtype=torch.bool)
+    if inner.dim() == buf.dim():
+        idx = [slice(None)] * (buf.dim() - 2) + [slice(1, -1), slice(None)]
+        m2 = torch.zeros_like(mask)
+        m2[tuple(idx)] = True
+        pad = (buf.shape[-1] - inner.shape[-1]) // 2
+        m3 = torch.zeros_like(mask)
+        m3[..., pad:pad + inner.shape[-1]] = True
+        mask = ~(m2 & m3)
+    return bool((b[mask] == CANARY).all())
+
+
+@pytest.mark.parametrize("pad", [8, 1])
+def test_outputs_write_nothing_outside_their_views(pad):
+    wl = W.WORKLOADS["tiny"]
+    # RoPE out-of-place into a padded (B, S, H, D) view
+    x = to_dev(W.rope_inputs(wl, "q"))
+    c, s = dt.rope_cos_sin_precompute(to_dev(W.freqs_for(wl)))
+    buf, out = _canvas(tuple(x.shape), pad)
+    dt.rope_rotate_half(x, c, s, out=out)
+    torch.cuda.synchronize()
+    assert _canary_intact(buf, out), "rope"
+    assert torch.equal(out.view(torch.int16), dt.rope_rotate_half(x, c, s).view(torch.int16))
+    # GEGLU into a padded (T, F) view
+    gu = to_dev(W.geglu_inputs(wl))
+    F = wl.F
+    buf, out = _canvas((wl.T_ff, F), pad)
+    dt.gelu_and_mul(gu[:, :F], gu[:, F:], out=out)
+    torch.cuda.synchronize()
+    assert _canary_intact(buf, out), "geglu"
+    # RMSNorm: padded out and a padded residual (updated in place)
+    xn, r, w = (to_dev(t) for t in W.rmsnorm_inputs(wl))
+    rbuf, rv = _canvas(tuple(r.shape), pad)
+    rv.copy_(r)
+    obuf, ov = _canvas(tuple(xn.shape), pad)
+    dt.rmsnorm_residual(xn, rv, w, EPS, out=ov)
+    torch.cuda.synchronize()
+    assert _canary_intact(rbuf, rv) and _canary_intact(obuf, ov), "rmsnorm"
+    # tables: contiguous outputs with canaries before and after
+    n = wl.tokens * wl.rot
+    cb = torch.full((n + 2 * pad,), CANARY, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    sb = torch.full((n + 2 * pad,), CANARY, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    dt.rope_cos_sin_precompute(to_dev(W.freqs_for(wl)), cb[pad:pad + n].view(wl.tokens, wl.rot),
+                               sb[pad:pad + n].view(wl.tokens, wl.rot))
+    torch.cuda.synchronize()
+    for t in (cb, sb):
+        v = t.view(torch.int16)
+        assert bool((v[:pad] == CANARY).all() and (v[pad + n:] == CANARY).all()), "tables"
