@@ -8,24 +8,34 @@
 // projection's accumulators before anything is stored, so gate_up never
 // reaches HBM: the call reads x and W and writes out.
 //
-// Design (one CTA per 128 x 128 output tile, tcgen05 tensor cores):
+// Design (tcgen05 tensor cores, persistent CTAs, warp-specialised):
 //   - the B operand of a tile is 256 weight rows: gate rows f0..f0+127 and up
-//     rows F+f0..F+f0+127, so one 128 x 256 fp32 accumulator in tensor memory
-//     holds gate and up of the same 128 output columns;
-//   - a kStages-deep ring of shared-memory stages (x: 128 x 64, W: 256 x 64
-//     bf16, 128-byte swizzle) filled by TMA (one thread) and consumed by
-//     tcgen05.mma (one thread, M 128, N 256, K 16 per instruction), with
-//     mbarriers for "stage full" (TMA transaction bytes) and "stage empty"
-//     (tcgen05.commit);
-//   - epilogue: each of the 4 warps reads its 32 accumulator lanes (rows) with
+//     rows F+f0..F+f0+127, so one fp32 accumulator row in tensor memory holds
+//     gate and up of the same 128 output columns;
+//   - a ring of shared-memory stages (x and W tiles, 64 columns of K, 128-byte
+//     swizzle) filled by TMA (one thread) and consumed by tcgen05.mma (one
+//     thread, K 16 per instruction), with mbarriers for "stage full" (TMA
+//     transaction bytes) and "stage empty" (tcgen05.commit);
+//   - two accumulators in tensor memory, so the epilogue of one tile overlaps
+//     the MMAs of the next;
+//   - epilogue: each of 4 warps reads its 32 accumulator lanes (rows) with
 //     tcgen05.ld, rounds gate and up to bf16 (the projection's output
 //     rounding), looks the activation up in a compact 17 KB table in shared
 //     memory and multiplies with one bf16x2 .rn multiply, as the standalone
 //     GEGLU kernel does;
 //   - optionally the rounded gate and up are stored too (a (T, 2F) gate_up
 //     tensor, for a backward pass or for checking);
-//   - tiles are visited in groups of 16 row tiles so that the x and W tiles a
+//   - tiles are visited in groups of row tiles so that the x and W tiles a
 //     wave of CTAs reads stay in L2.
+// Two kernels share this design:
+//   gemm_geglu_pair_kernel  CTA pairs (clusters of 2 on the two SMs of a TPC)
+//       with cta_group::2 MMAs of M 256 x N 256: each CTA stages 128 rows of x
+//       and 128 rows of W (the first CTA the gate rows, the second the up
+//       rows), 32 KB per stage, so a pair reads half the W bytes two single
+//       CTAs would and six stages fit in shared memory;
+//   gemm_geglu_kernel  one CTA per 128-row tile, M 128 x N 256, 48 KB stages,
+//       for T <= 128 (a pair tile would be half empty) or when no cluster of
+//       two fits.
 // Every mbarrier wait is bounded (about a second of %globaltimer): a wait that
 // runs out records a code in the workspace's error word and the CTA finishes
 // without further waits; later CTAs that see the word set exit at once.
@@ -62,7 +72,17 @@ constexpr uint32_t kErrOffset = kTabBytes;                     // error word in 
 constexpr uint32_t kWorkspaceBytes = 17408;
 
 constexpr uint32_t kErrTimeoutEmpty = 1, kErrTimeoutFull = 2, kErrTimeoutAccum = 4;
+constexpr uint32_t kErrTmemMismatch = 8;  // the two CTAs of a pair got different columns
 constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any single wait
+
+// CTA pairs: a pair tile is 256 output rows (128 per CTA) x 128 output columns
+constexpr int kStagesP = 6;
+constexpr int kGroupMP = 8;                       // pair row tiles per raster group
+constexpr uint32_t kAHalf = BM * BK * 2;          // 16 KB: this CTA's 128 rows of x
+constexpr uint32_t kBHalf = BNH * BK * 2;         // 16 KB: this CTA's 128 rows of W
+constexpr uint32_t kStageBytesP = kAHalf + kBHalf;
+constexpr uint32_t kPairTx = 2 * kStageBytesP;    // bytes both CTAs land per stage
+constexpr uint16_t kBothCtas = 0x3;               // multicast mask of a pair
 
 struct GemmGegluParams {
     uint16_t* out;
@@ -181,6 +201,96 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- CTA-pair helpers
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs: release this CTA's earlier shared-memory writes
+// and wait for the peer's.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (the barrier may receive arrivals
+// and transaction bytes from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, uint32_t* err,
+                                             uint32_t code) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait_cl(bar, parity)) {
+        if (global_ns() - t0 > kWaitNs) {
+            atomicOr(err, code);
+            return false;
+        }
+    }
+    return true;
+}
+// TMA load into this CTA's shared memory whose transaction bytes complete on
+// `bar_cluster`, an mbarrier of this CTA or of its peer.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+// Instruction descriptor of the pair MMA: as kIdesc with M = 256.
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
+
+// D[256 x 256] (+)= A[256 x 16] B[16 x 256]: A rows 0-127 and B rows (N)
+// 0-127 are read from the issuing CTA's shared memory, A rows 128-255 and B
+// rows 128-255 from the same addresses in the peer; D rows 0-127 land in the
+// issuing CTA's tensor memory, rows 128-255 in the peer's.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(kIdescPair), "r"(acc)
+        : "memory");
+}
+// Arrive once on the mbarrier at `bar`'s offset in both CTAs of the pair when
+// the pair MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(kBothCtas)
+        : "memory");
+}
+// The same, on this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- activation
 
 // g(x) = RN16(RN32(gelu(x))) for the bf16 pattern b, from the compact table or
@@ -220,13 +330,79 @@ __global__ void __launch_bounds__(256) gelu_compact_table_kernel(uint16_t* __res
 // ---------------------------------------------------------------- the GEMM
 
 // Tile t of the grouped order: row tiles advance fastest within a group of
-// kGroupM, so the CTAs working at the same time share x and W tiles in L2.
+// kGroup, so the CTAs working at the same time share x and W tiles in L2.
+template <int kRows, int kGroup>
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& m0, int& f0) {
-    const int in_group = kGroupM * num_n;
-    const int first_m = (t / in_group) * kGroupM;
-    const int gm = min(num_m - first_m, kGroupM);
-    m0 = (first_m + (t % in_group) % gm) * BM;
+    const int in_group = kGroup * num_n;
+    const int first_m = (t / in_group) * kGroup;
+    const int gm = min(num_m - first_m, kGroup);
+    m0 = (first_m + (t % in_group) % gm) * kRows;
     f0 = ((t % in_group) / gm) * BNH;
+}
+
+// Epilogue of one accumulator row (this thread's lane): gate in columns
+// 0..127 of `taddr`, up in 128..255; output columns f0..f0+127 of `row`.
+__device__ __forceinline__ void epilogue_row(const GemmGegluParams& p, const uint16_t* tab,
+                                             uint32_t taddr, int64_t row, int f0) {
+#pragma unroll 1
+    for (int j = 0; j < BNH / 32; ++j) {
+        uint32_t g[32], u[32];
+        tmem_ld32(taddr + 32 * j, g);
+        tmem_ld32(taddr + BNH + 32 * j, u);
+        tmem_wait_ld();
+        if (row < p.T) {
+            uint32_t o[16], gb[16], ub[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                gb[q] = rn16x2f(__uint_as_float(g[2 * q]), __uint_as_float(g[2 * q + 1]));
+                ub[q] = rn16x2f(__uint_as_float(u[2 * q]), __uint_as_float(u[2 * q + 1]));
+                o[q] = bmul2(ub[q], gelu_lookup2(tab, gb[q]));
+            }
+            uint16_t* dst = p.out + row * p.s_out + f0 + 32 * j;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (f0 + 32 * j + 8 * q < p.F)
+                    *reinterpret_cast<uint4*>(dst + 8 * q) =
+                        make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
+            if (p.gate_up) {
+                uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (f0 + 32 * j + 8 * q < p.F) {
+                        *reinterpret_cast<uint4*>(gdst + 8 * q) =
+                            make_uint4(gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
+                        *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) =
+                            make_uint4(ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Copy the compact activation table from the workspace into shared memory.
+__device__ __forceinline__ void load_table(const GemmGegluParams& p, uint16_t* tab) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.table);
+    uint4* dst = reinterpret_cast<uint4*>(tab);
+    for (int i = threadIdx.x; i < (int)(kTabBytes / 16); i += kThreads) dst[i] = __ldcg(src + i);
+}
+
+// The producer's last loads must have landed before the CTA exits (on the
+// normal path the MMAs consumed them; after an abort they may be in flight).
+// `issued` counts the stage uses this thread filled.
+template <int kNumStages>
+__device__ __forceinline__ void wait_own_loads(uint32_t full0, uint32_t issued, uint32_t* err,
+                                               bool cluster_scope) {
+    const uint32_t n = issued < (uint32_t)kNumStages ? issued : (uint32_t)kNumStages;
+    for (uint32_t i = 0; i < n; ++i) {
+        const uint32_t use = issued - 1 - i;
+        const uint32_t bar = full0 + 8 * (use % kNumStages);
+        const uint32_t ph = (use / kNumStages) & 1u;
+        if (cluster_scope ? !mbar_wait_cl(bar, ph, err, kErrTimeoutFull)
+                          : !mbar_wait(bar, ph, err, kErrTimeoutFull))
+            return;
+    }
 }
 
 // Persistent CTAs (one per SM) walk tiles blockIdx.x, blockIdx.x + gridDim.x, ...
@@ -290,11 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(p.table);
-        uint4* dst = reinterpret_cast<uint4*>(tab);
-        for (int i = threadIdx.x; i < (int)(kTabBytes / 16); i += kThreads) dst[i] = __ldcg(src + i);
-    }
+    load_table(p, tab);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
@@ -305,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             for (int t = blockIdx.x; t < tiles && !s_abort; t += gridDim.x) {
                 int m0, f0;
-                tile_coords(t, p.num_m, p.num_n, m0, f0);
-                for (int kb = 0; kb < nk; ++kb, ++it) {
+                tile_coords<BM, kGroupM>(t, p.num_m, p.num_n, m0, f0);
+                for (int kb = 0; kb < nk; ++kb) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (it >= (uint32_t)kStages &&
@@ -320,8 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(sB + s * kBTile, &tma_w, kb * BK, f0, fb);
                     tma_load_2d(sB + s * kBTile + BNH * BK * 2, &tma_w, kb * BK,
                                 (int32_t)p.F + f0, fb);
+                    ++it;
                 }
             }
+            wait_own_loads<kStages>(full0, it, p.err, false);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -379,44 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             int m0, f0;
-            tile_coords(t, p.num_m, p.num_n, m0, f0);
+            tile_coords<BM, kGroupM>(t, p.num_m, p.num_n, m0, f0);
             const int64_t row = (int64_t)m0 + quarter * 32 + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols;
-#pragma unroll 1
-            for (int j = 0; j < BNH / 32; ++j) {
-                uint32_t g[32], u[32];
-                tmem_ld32(taddr + 32 * j, g);
-                tmem_ld32(taddr + BNH + 32 * j, u);
-                tmem_wait_ld();
-                if (row < p.T) {
-                    uint32_t o[16], gb[16], ub[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        gb[q] = rn16x2f(__uint_as_float(g[2 * q]), __uint_as_float(g[2 * q + 1]));
-                        ub[q] = rn16x2f(__uint_as_float(u[2 * q]), __uint_as_float(u[2 * q + 1]));
-                        o[q] = bmul2(ub[q], gelu_lookup2(tab, gb[q]));
-                    }
-                    uint16_t* dst = p.out + row * p.s_out + f0 + 32 * j;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (f0 + 32 * j + 8 * q < p.F)
-                            *reinterpret_cast<uint4*>(dst + 8 * q) =
-                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                    }
-                    if (p.gate_up) {
-                        uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (f0 + 32 * j + 8 * q < p.F) {
-                                *reinterpret_cast<uint4*>(gdst + 8 * q) = make_uint4(
-                                    gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
-                                *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) = make_uint4(
-                                    ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
-                            }
-                        }
-                    }
-                }
-            }
+            epilogue_row(p, tab,
+                         tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols, row,
+                         f0);
             // this accumulator may be overwritten once all four warps are done
             tc_fence_before();
             __syncwarp();
@@ -433,11 +574,195 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
 }
 
+// CTA pairs (clusters of 2).  Both CTAs of a cluster walk the same pair tiles
+// (cluster c takes tiles c, c + clusters, ...).  Roles as in gemm_geglu_kernel,
+// except that:
+//   - each CTA's producer loads its own 128 rows of x and 128 rows of W (rank
+//     0 the gate rows, rank 1 the up rows) into its own shared memory, and
+//     both signal rank 0's full barrier, whose expected byte count (set by
+//     rank 0's producer) covers the two CTAs;
+//   - only rank 0's MMA thread issues (cta_group::2, M 256 x N 256); its
+//     commits arrive on the empty and acc_full barriers of both CTAs;
+//   - the epilogue warps of both CTAs arrive on rank 0's acc_empty barrier
+//     (8 arrivals per phase);
+//   - tensor memory is allocated and freed by one warp of each CTA together;
+//   - a cluster barrier after the set-up (the peer signals rank 0's barriers,
+//     which must be initialised first) and one before the exit (no CTA leaves
+//     while the other may still signal its barriers or read its stages).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_geglu_pair_kernel(const __grid_constant__ CUtensorMap tma_x,
+                           const __grid_constant__ CUtensorMap tma_w, GemmGegluParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ volatile uint32_t s_abort;
+    // the table kernel (the prerequisite grid) has written the activation table
+    // and cleared the error word once this returns
+    wait_for_prerequisite_grid();
+
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // the same offset in both CTAs
+    uint8_t* sm = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + kStagesP * kAHalf;
+    uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStagesP * kStageBytesP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStagesP * kStageBytesP + kTabBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesP + 5);
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStagesP;
+    const uint32_t acc_full0 = full0 + 16 * kStagesP, acc_empty0 = acc_full0 + 16;
+    const uint32_t drain = acc_empty0 + 16;  // every MMA issued by rank 0 has completed
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cluster = (int)(blockIdx.x >> 1), clusters = (int)(gridDim.x >> 1);
+    const int tiles = p.num_m * p.num_n;  // num_m counts 256-row pair tiles
+    const int nk = (int)((p.C + BK - 1) / BK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesP; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full0 + 8 * a, 1);
+            mbar_init(acc_empty0 + 8 * a, 8);
+        }
+        mbar_init(drain, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    load_table(p, tab);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (rank == 1 && threadIdx.x == 0) {
+        // the pair MMAs write rank 1's rows at rank 0's tensor-memory address
+        uint32_t lead;
+        asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                     : "=r"(lead)
+                     : "r"(peer_addr(smem_u32(tmem_slot), 0))
+                     : "memory");
+        if (lead != tmem) atomicOr(p.err, kErrTmemMismatch);
+    }
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // TMA producer of this CTA's half of every stage
+            const uint32_t full_lead0 = peer_addr(full0, 0);
+            uint32_t it = 0;
+            for (int t = cluster; t < tiles && !s_abort; t += clusters) {
+                int m0, f0;
+                tile_coords<2 * BM, kGroupMP>(t, p.num_m, p.num_n, m0, f0);
+                const int32_t xrow = m0 + (int32_t)rank * BM;
+                const int32_t wrow = (rank ? (int32_t)p.F : 0) + f0;
+                for (int kb = 0; kb < nk; ++kb) {
+                    const uint32_t s = it % kStagesP;
+                    const uint32_t ph = (it / kStagesP) & 1u;
+                    if (it >= (uint32_t)kStagesP &&
+                        !mbar_wait_cl(empty0 + 8 * s, ph ^ 1u, p.err, kErrTimeoutEmpty)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    if (rank == 0) mbar_expect_tx(full0 + 8 * s, kPairTx);
+                    tma_load_2d_pair(sA + s * kAHalf, &tma_x, kb * BK, xrow, full_lead0 + 8 * s);
+                    tma_load_2d_pair(sB + s * kBHalf, &tma_w, kb * BK, wrow, full_lead0 + 8 * s);
+                    ++it;
+                }
+            }
+            // rank 0's full barriers also count rank 1's bytes
+            if (rank == 0) wait_own_loads<kStagesP>(full0, it, p.err, true);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // MMA issuer for the pair: 4 instructions of K 16 per stage into
+            // accumulator i % 2 of both CTAs
+            uint32_t it = 0;
+            int i = 0;
+            for (int t = cluster; t < tiles && !s_abort; t += clusters, ++i) {
+                const int acc = i & 1;
+                if (i >= 2 && !mbar_wait_cl(acc_empty0 + 8 * acc, ((i >> 1) & 1) ^ 1, p.err,
+                                            kErrTimeoutAccum)) {
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)acc * kAccCols;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % kStagesP;
+                    const uint32_t ph = (it / kStagesP) & 1u;
+                    if (!mbar_wait_cl(full0 + 8 * s, ph, p.err, kErrTimeoutFull)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a = smem_desc(sA + s * kAHalf);
+                    const uint64_t b = smem_desc(sB + s * kBHalf);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16_pair(d, a + 2 * k, b + 2 * k, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit_pair(empty0 + 8 * s);
+                }
+                mma_commit_pair(acc_full0 + 8 * acc);
+                if (s_abort) break;
+            }
+            mma_commit_pair_local(drain);
+            mbar_wait(drain, 0, p.err, kErrTimeoutAccum);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: warp w reads accumulator lanes 32 * (w % 4) .. + 31, the
+        // rows rank * 128 + lane of the pair tile
+        const int quarter = warp & 3;
+        const uint32_t acc_empty_lead0 = peer_addr(acc_empty0, 0);
+        int i = 0;
+        for (int t = cluster; t < tiles; t += clusters, ++i) {
+            const int acc = i & 1;
+            const bool ok = !s_abort && mbar_wait_cl(acc_full0 + 8 * acc, (i >> 1) & 1, p.err,
+                                                     kErrTimeoutAccum);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, ok)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            int m0, f0;
+            tile_coords<2 * BM, kGroupMP>(t, p.num_m, p.num_n, m0, f0);
+            const int64_t row = (int64_t)m0 + (int64_t)rank * BM + quarter * 32 + lane;
+            epilogue_row(p, tab,
+                         tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols, row,
+                         f0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acc_empty_lead0 + 8 * acc);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
 constexpr size_t kSmemBytes =
     1024 + (size_t)kStages * kStageBytes + kTabBytes + (2 * kStages + 5) * 8 + 16;
+constexpr size_t kSmemBytesP =
+    1024 + (size_t)kStagesP * kStageBytesP + kTabBytes + (2 * kStagesP + 5) * 8 + 16;
 
 constexpr int kMaxDev = 64;
 std::atomic<bool> g_smem_attr[kMaxDev];
+// per device: co-resident clusters of the pair kernel + 1 (0: not asked yet)
+std::atomic<int> g_pair_clusters[kMaxDev];
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -475,6 +800,24 @@ bool make_map(CUtensorMap* m, const uint16_t* ptr, int64_t rows, int64_t cols) {
            CUDA_SUCCESS;
 }
 
+// Clusters of two pair-kernel CTAs that fit on the device at once (0: none).
+cudaError_t pair_clusters(int dev, int* out) {
+    int c = g_pair_clusters[dev].load(std::memory_order_acquire);
+    if (c == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytesP;
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, gemm_geglu_pair_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        c = (n > 0 ? n : 0) + 1;
+        g_pair_clusters[dev].store(c, std::memory_order_release);
+    }
+    *out = c - 1;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 size_t gemm_geglu_workspace_bytes() { return kWorkspaceBytes; }
@@ -487,6 +830,9 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     if (!g_smem_attr[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(gemm_geglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm_geglu_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
         if (e != cudaSuccess) return e;
         g_smem_attr[dev].store(true, std::memory_order_release);
     }
@@ -510,11 +856,26 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     p.F = a.F;
     p.table = table;
     p.err = err;
-    p.num_m = (int)((a.T + BM - 1) / BM);
     p.num_n = (int)((a.F + BNH - 1) / BNH);
-    const int64_t tiles = (int64_t)p.num_m * p.num_n;
-    int64_t grid = num_sms();  // persistent: one CTA per SM (the stage ring fills its smem)
-    if (grid > tiles) grid = tiles;
+
+    // CTA pairs unless a pair tile would be half empty or no cluster fits
+    int clusters = 0;
+    if (a.T > BM) {
+        e = pair_clusters(dev, &clusters);
+        if (e != cudaSuccess) return e;
+    }
+    const bool pair = clusters > 0;
+    int64_t grid;
+    if (pair) {
+        p.num_m = (int)((a.T + 2 * BM - 1) / (2 * BM));
+        const int64_t tiles = (int64_t)p.num_m * p.num_n;
+        grid = 2 * (tiles < clusters ? tiles : (int64_t)clusters);
+    } else {
+        p.num_m = (int)((a.T + BM - 1) / BM);
+        const int64_t tiles = (int64_t)p.num_m * p.num_n;
+        grid = num_sms();  // persistent: one CTA per SM (the stage ring fills its smem)
+        if (grid > tiles) grid = tiles;
+    }
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -522,11 +883,12 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = pair ? kSmemBytesP : kSmemBytes;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_geglu_kernel, mx, mw, p);
+    e = pair ? cudaLaunchKernelEx(&cfg, gemm_geglu_pair_kernel, mx, mw, p)
+             : cudaLaunchKernelEx(&cfg, gemm_geglu_kernel, mx, mw, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
