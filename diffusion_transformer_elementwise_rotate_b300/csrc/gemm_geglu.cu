@@ -59,6 +59,9 @@ constexpr uint32_t kATile = BM * BK * 2;   // 16 KB
 constexpr uint32_t kBTile = BN * BK * 2;   // 32 KB
 constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr uint32_t kAccCols = 256;   // one 128 x 256 fp32 accumulator
+// output staging for TMA stores: per epilogue warp two 32 x 32 bf16 blocks
+constexpr uint32_t kOutBlock = 32 * 32 * 2;          // 2 KB
+constexpr uint32_t kOutStaging = 4 * 2 * kOutBlock;  // 16 KB
 constexpr uint32_t kTmemCols = 512;  // two accumulators: MMA and epilogue overlap
 
 // Compact activation table: entries for |x| in [2^-30, 8) (x > 0) and
@@ -77,7 +80,11 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any single wait
 
 // CTA pairs: a pair tile is 256 output rows (128 per CTA) x 128 output columns
 constexpr int kStagesP = 6;
-constexpr int kGroupMP = 8;                       // pair row tiles per raster group
+// pair row tiles per raster group: a wave of 74 clusters covers 16 pair rows x
+// ~5 column tiles, and W is re-read from DRAM once per 4096 rows (at the power
+// limit the DRAM traffic saved is worth more than the smaller wave footprint
+// of groups of 8)
+constexpr int kGroupMP = 16;
 constexpr uint32_t kAHalf = BM * BK * 2;          // 16 KB: this CTA's 128 rows of x
 constexpr uint32_t kBHalf = BNH * BK * 2;         // 16 KB: this CTA's 128 rows of W
 constexpr uint32_t kStageBytesP = kAHalf + kBHalf;
@@ -143,6 +150,36 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+// TMA store of a 32 x 32 block from shared memory (rows >= T and columns >= F
+// of the tensor map are not written).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most one store group of this thread still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Every store group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -225,13 +262,18 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// The waiting thread sleeps in hardware until the phase completes or
+// kSuspendNs pass (a spinning wait costs issue slots and power, and the pair
+// kernel runs at the power limit).
+constexpr uint32_t kSuspendNs = 1000000u;
 __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -303,11 +345,19 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
 //   x <= -16: |gelu(x)| < 1e-55 < 2^-150, so RN32 gives -0; -inf gives NaN
 //       (-inf * 0) like the formula.
 __device__ __forceinline__ uint32_t gelu_lookup(const uint16_t* tab, uint32_t b) {
-    const uint32_t e = (b >> 7) & 0xFFu;
-    if (e < (uint32_t)kExpLo) return rn16f(__fmul_rn(__uint_as_float(b << 16), 0.5f));
-    if (!(b & 0x8000u)) return e >= 130 ? b : tab[(b & 0x7FFFu) - (kExpLo << 7)];
-    if (e >= 131) return e == 255 ? 0x7FC0u : 0x8000u;
-    return tab[kPosEntries + (b & 0x7FFFu) - (kExpLo << 7)];
+    // without branches: one table load at a clamped index, then the closed
+    // forms by selection (b is a 16-bit pattern; m = |x|'s pattern, whose
+    // exponent field compares like m against e << 7)
+    const uint32_t m = b & 0x7FFFu;
+    const uint32_t neg = b >> 15;
+    int idx = (int)m - (kExpLo << 7) + (int)neg * kPosEntries;
+    idx = min(max(idx, 0), kCompact - 1);
+    uint32_t r = tab[idx];
+    const uint32_t half = rn16f(__fmul_rn(__uint_as_float(b << 16), 0.5f));
+    r = m < ((uint32_t)kExpLo << 7) ? half : r;
+    r = (!neg && m >= (130u << 7)) ? b : r;
+    r = (neg && m >= (131u << 7)) ? (m >= (255u << 7) ? 0x7FC0u : 0x8000u) : r;
+    return r;
 }
 
 __device__ __forceinline__ uint32_t gelu_lookup2(const uint16_t* tab, uint32_t g2) {
@@ -340,44 +390,63 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& m0
     f0 = ((t % in_group) / gm) * BNH;
 }
 
-// Epilogue of one accumulator row (this thread's lane): gate in columns
-// 0..127 of `taddr`, up in 128..255; output columns f0..f0+127 of `row`.
-__device__ __forceinline__ void epilogue_row(const GemmGegluParams& p, const uint16_t* tab,
-                                             uint32_t taddr, int64_t row, int f0) {
+// Epilogue of one warp's 32 accumulator rows (lane = row row0 + lane): gate in
+// columns 0..127 of `taddr`, up in 128..255; output columns f0..f0+127.  Each
+// 32 x 32 output block goes through one of the warp's two staging buffers in
+// shared memory (`stage0`, 2 x 2 KB) and out by TMA store, 64-byte row
+// segments instead of 16-byte pieces of 32 rows.  The staging rows use the
+// 64-byte swizzle of the output tensor map (16-byte chunk c of row r at
+// chunk c ^ ((r >> 1) & 3)), so the 32 lanes' writes hit distinct banks.
+// `nstore` counts this warp's stores (it picks the buffer).
+__device__ __forceinline__ void epilogue_rows(const GemmGegluParams& p, const uint16_t* tab,
+                                              const CUtensorMap* tma_out, uint32_t taddr,
+                                              int64_t row0, int f0, uint32_t stage0,
+                                              uint32_t& nstore) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = row0 + lane;
+    const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
 #pragma unroll 1
     for (int j = 0; j < BNH / 32; ++j) {
         uint32_t g[32], u[32];
         tmem_ld32(taddr + 32 * j, g);
         tmem_ld32(taddr + BNH + 32 * j, u);
         tmem_wait_ld();
-        if (row < p.T) {
-            uint32_t o[16], gb[16], ub[16];
+        uint32_t o[16], gb[16], ub[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                gb[q] = rn16x2f(__uint_as_float(g[2 * q]), __uint_as_float(g[2 * q + 1]));
-                ub[q] = rn16x2f(__uint_as_float(u[2 * q]), __uint_as_float(u[2 * q + 1]));
-                o[q] = bmul2(ub[q], gelu_lookup2(tab, gb[q]));
-            }
-            uint16_t* dst = p.out + row * p.s_out + f0 + 32 * j;
+        for (int q = 0; q < 16; ++q) {
+            gb[q] = rn16x2f(__uint_as_float(g[2 * q]), __uint_as_float(g[2 * q + 1]));
+            ub[q] = rn16x2f(__uint_as_float(u[2 * q]), __uint_as_float(u[2 * q + 1]));
+            o[q] = bmul2(ub[q], gelu_lookup2(tab, gb[q]));
+        }
+        if (p.gate_up && row < p.T) {
+            uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if (f0 + 32 * j + 8 * q < p.F)
-                    *reinterpret_cast<uint4*>(dst + 8 * q) =
-                        make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            }
-            if (p.gate_up) {
-                uint16_t* gdst = p.gate_up + row * p.s_gate_up + f0 + 32 * j;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (f0 + 32 * j + 8 * q < p.F) {
-                        *reinterpret_cast<uint4*>(gdst + 8 * q) =
-                            make_uint4(gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
-                        *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) =
-                            make_uint4(ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
-                    }
+                if (f0 + 32 * j + 8 * q < p.F) {
+                    *reinterpret_cast<uint4*>(gdst + 8 * q) =
+                        make_uint4(gb[4 * q], gb[4 * q + 1], gb[4 * q + 2], gb[4 * q + 3]);
+                    *reinterpret_cast<uint4*>(gdst + p.F + 8 * q) =
+                        make_uint4(ub[4 * q], ub[4 * q + 1], ub[4 * q + 2], ub[4 * q + 3]);
                 }
             }
         }
+        const uint32_t buf = stage0 + (nstore & 1u) * kOutBlock;
+        // the store that used this buffer two blocks ago has read it
+        if (lane == 0) bulk_wait_read_1();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            st_shared_v4(buf + (uint32_t)lane * 64 + (((uint32_t)c ^ sw) << 4), o[4 * c],
+                         o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        fence_async_smem();
+        __syncwarp();
+        // a block wholly past the last row or column is not stored (partial
+        // blocks are clipped by the tensor map)
+        if (lane == 0 && row0 < p.T && f0 + 32 * j < p.F) {
+            tma_store_2d(tma_out, buf, f0 + 32 * j, (int32_t)row0);
+            bulk_commit();
+        }
+        ++nstore;
     }
 }
 
@@ -415,7 +484,8 @@ __device__ __forceinline__ void wait_own_loads(uint32_t full0, uint32_t issued, 
 // time sets `abort` in shared memory and every role leaves its loop.
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_geglu_kernel(const __grid_constant__ CUtensorMap tma_x,
-                      const __grid_constant__ CUtensorMap tma_w, GemmGegluParams p) {
+                      const __grid_constant__ CUtensorMap tma_w,
+                      const __grid_constant__ CUtensorMap tma_out, GemmGegluParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_skip;
     __shared__ volatile uint32_t s_abort;
@@ -436,8 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sm = smem_raw + (base - raw);
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * kATile;
-    uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStages * kStageBytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStages * kStageBytes + kTabBytes);
+    const uint32_t sOut = base + kStages * kStageBytes;  // output staging, 1024-byte aligned
+    uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStages * kStageBytes + kOutStaging);
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(sm + kStages * kStageBytes + kOutStaging + kTabBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStages;
     const uint32_t acc_full0 = full0 + 16 * kStages, acc_empty0 = acc_full0 + 16;
@@ -541,6 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // epilogue: warp w reads accumulator lanes 32 * (w % 4) .. + 31
         const int quarter = warp & 3;
+        const uint32_t stage0 = sOut + (uint32_t)quarter * 2 * kOutBlock;
+        uint32_t nstore = 0;
         int i = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
             const int acc = i & 1;
@@ -554,10 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             int m0, f0;
             tile_coords<BM, kGroupM>(t, p.num_m, p.num_n, m0, f0);
-            const int64_t row = (int64_t)m0 + quarter * 32 + lane;
-            epilogue_row(p, tab,
-                         tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols, row,
-                         f0);
+            epilogue_rows(p, tab, &tma_out,
+                          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols,
+                          (int64_t)m0 + quarter * 32, f0, stage0, nstore);
             // this accumulator may be overwritten once all four warps are done
             tc_fence_before();
             __syncwarp();
@@ -565,6 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             acc_empty0 + 8 * acc)
                                         : "memory");
         }
+        // the stores have read the staging buffers and written the output
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -591,7 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 //     while the other may still signal its barriers or read its stages).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_geglu_pair_kernel(const __grid_constant__ CUtensorMap tma_x,
-                           const __grid_constant__ CUtensorMap tma_w, GemmGegluParams p) {
+                           const __grid_constant__ CUtensorMap tma_w,
+                           const __grid_constant__ CUtensorMap tma_out, GemmGegluParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ volatile uint32_t s_abort;
     // the table kernel (the prerequisite grid) has written the activation table
@@ -604,8 +681,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* sm = smem_raw + (base - raw);
     const uint32_t sA = base;
     const uint32_t sB = base + kStagesP * kAHalf;
-    uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStagesP * kStageBytesP);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStagesP * kStageBytesP + kTabBytes);
+    const uint32_t sOut = base + kStagesP * kStageBytesP;  // output staging, 1024-byte aligned
+    uint16_t* tab = reinterpret_cast<uint16_t*>(sm + kStagesP * kStageBytesP + kOutStaging);
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(sm + kStagesP * kStageBytesP + kOutStaging + kTabBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesP + 5);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStagesP;
     const uint32_t acc_full0 = full0 + 16 * kStagesP, acc_empty0 = acc_full0 + 16;
@@ -722,6 +801,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // rows rank * 128 + lane of the pair tile
         const int quarter = warp & 3;
         const uint32_t acc_empty_lead0 = peer_addr(acc_empty0, 0);
+        const uint32_t stage0 = sOut + (uint32_t)quarter * 2 * kOutBlock;
+        uint32_t nstore = 0;
         int i = 0;
         for (int t = cluster; t < tiles; t += clusters, ++i) {
             const int acc = i & 1;
@@ -735,14 +816,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             int m0, f0;
             tile_coords<2 * BM, kGroupMP>(t, p.num_m, p.num_n, m0, f0);
-            const int64_t row = (int64_t)m0 + (int64_t)rank * BM + quarter * 32 + lane;
-            epilogue_row(p, tab,
-                         tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols, row,
-                         f0);
+            epilogue_rows(p, tab, &tma_out,
+                          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kAccCols,
+                          (int64_t)m0 + (int64_t)rank * BM + quarter * 32, f0, stage0, nstore);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(acc_empty_lead0 + 8 * acc);
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -754,10 +836,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                      : "memory");
 }
 
-constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kStageBytes + kTabBytes + (2 * kStages + 5) * 8 + 16;
-constexpr size_t kSmemBytesP =
-    1024 + (size_t)kStagesP * kStageBytesP + kTabBytes + (2 * kStagesP + 5) * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kOutStaging + kTabBytes +
+                              (2 * kStages + 5) * 8 + 16;
+constexpr size_t kSmemBytesP = 1024 + (size_t)kStagesP * kStageBytesP + kOutStaging + kTabBytes +
+                               (2 * kStagesP + 5) * 8 + 16;
+static_assert(kSmemBytes <= 232448 && kSmemBytesP <= 232448, "shared memory per CTA");
 
 constexpr int kMaxDev = 64;
 std::atomic<bool> g_smem_attr[kMaxDev];
@@ -800,6 +883,21 @@ bool make_map(CUtensorMap* m, const uint16_t* ptr, int64_t rows, int64_t cols) {
            CUDA_SUCCESS;
 }
 
+// The output (rows, cols) with row stride `stride` elements, 32 x 32 boxes,
+// 64-byte swizzle (the staging layout of epilogue_rows).
+bool make_out_map(CUtensorMap* m, uint16_t* ptr, int64_t rows, int64_t cols, int64_t stride) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Clusters of two pair-kernel CTAs that fit on the device at once (0: none).
 cudaError_t pair_clusters(int dev, int* out) {
     int c = g_pair_clusters[dev].load(std::memory_order_acquire);
@@ -836,8 +934,9 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         g_smem_attr[dev].store(true, std::memory_order_release);
     }
-    CUtensorMap mx, mw;
-    if (!make_map(&mx, a.x, a.T, a.C) || !make_map(&mw, a.w, 2 * a.F, a.C))
+    CUtensorMap mx, mw, mo;
+    if (!make_map(&mx, a.x, a.T, a.C) || !make_map(&mw, a.w, 2 * a.F, a.C) ||
+        !make_out_map(&mo, a.out, a.T, a.F, a.s_out))
         return cudaErrorInvalidValue;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     uint16_t* table = reinterpret_cast<uint16_t*>(ws);
@@ -887,8 +986,8 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = pair ? cudaLaunchKernelEx(&cfg, gemm_geglu_pair_kernel, mx, mw, p)
-             : cudaLaunchKernelEx(&cfg, gemm_geglu_kernel, mx, mw, p);
+    e = pair ? cudaLaunchKernelEx(&cfg, gemm_geglu_pair_kernel, mx, mw, mo, p)
+             : cudaLaunchKernelEx(&cfg, gemm_geglu_kernel, mx, mw, mo, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
