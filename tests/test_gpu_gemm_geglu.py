@@ -55,8 +55,12 @@ def _check_workspace_error_word():
     assert err == 0, f"a wait inside the kernel ran out of time (code {err})"
 
 
+# T <= 128 runs one CTA per 128-row tile; larger T runs CTA pairs (256-row
+# tiles): T = 129 leaves the second CTA of the pair one valid row, and F = 40 or
+# 264 ends the output inside a 32-column store block.
 @pytest.mark.parametrize("T,C,F", [(128, 64, 128), (300, 512, 256), (257, 1000, 200),
-                                   (33, 4096, 384), (1, 8, 8)])
+                                   (33, 4096, 384), (1, 8, 8), (129, 192, 40),
+                                   (255, 320, 264), (640, 128, 1000)])
 def test_exact_inputs_bitexact(T, C, F):
     x = _grid_values((T, C), T + C)
     w = _grid_values((2 * F, C), F + 7)
