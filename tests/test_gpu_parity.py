@@ -6,6 +6,8 @@ be bit-exact by design; the mismatch count is printed).  Inputs are the seeded
 synthetic workloads; the full-size video layer runs in the launch
 configuration the benchmark times and is checked on sampled rows.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -68,6 +70,25 @@ def test_cos_sin_many_angles_near_rounding_midpoints():
     # 4M angles spread over the position * frequency range of the workloads
     g = torch.Generator().manual_seed(5)
     f = (torch.rand(1 << 22, generator=g) * 60.0 - 5.0).view(-1, 1, 1, 64)
+    c, s = dt.rope_cos_sin_precompute(to_dev(f))
+    ec, es = oracle.rope_cos_sin(f.numpy())
+    assert_bitexact(bits(c), ec, "cos")
+    assert_bitexact(bits(s), es, "sin")
+
+
+def test_cos_sin_reduction_range_and_zero_crossings():
+    # Angles where the table kernel's hardware sine/cosine path ends: uniform over
+    # [-4100, 4100] (that path reduces |f| <= 4096 by 2 pi), next to every multiple
+    # of pi/2 up to 4096 (zeros of sin and cos, and the ends of the reduced
+    # range), and the float32 neighbours of +-4096.
+    g = torch.Generator().manual_seed(23)
+    u = torch.rand(1 << 21, generator=g, dtype=torch.float64) * 8200.0 - 4100.0
+    base = torch.arange(-2608, 2609, dtype=torch.float64) * (math.pi / 2)
+    near = torch.cat([base + d for d in (-1e-3, -3e-5, -1e-6, 0.0, 1e-6, 3e-5, 1e-3)])
+    e = np.array([4096.0, -4096.0], dtype=np.float32)
+    edge = np.concatenate([e, np.nextafter(e, np.float32(0)), np.nextafter(e, e * 2)])
+    f = torch.cat([u.to(torch.float32), near.to(torch.float32), torch.from_numpy(edge)])
+    f = f[: (f.numel() // 8) * 8].reshape(-1, 1, 1, 8).contiguous()
     c, s = dt.rope_cos_sin_precompute(to_dev(f))
     ec, es = oracle.rope_cos_sin(f.numpy())
     assert_bitexact(bits(c), ec, "cos")
