@@ -424,7 +424,7 @@ DTROT_API dtrot_status dtrot_gelu_and_mul_with_table(const uint16_t* gate, int64
         return DTROT_ERR_ALIAS;
     if (!device_ok()) return DTROT_ERR_DEVICE;
     return launch_status(
-        launch_gelu_stream(p, (const uint16_t*)table, false, (cudaStream_t)stream));
+        launch_gelu_stream(p, (const uint16_t*)table, (cudaStream_t)stream));
 }
 
 // GEGLU for callers that cannot allocate device memory: the same computation

@@ -186,6 +186,39 @@ struct RmsParams {
     float eps;
 };
 
+// ------------------------------------------------------------ launch order
+//
+// The library's kernels are launched as programmatic dependents of the
+// previous kernel in the stream: a launch may be scheduled while its
+// predecessor finishes, which hides the launch and ramp-up between the short
+// memory-bound kernels of a step.  Every kernel therefore executes pdl_wait()
+// before its first global-memory access, read or write; pdl_wait returns once
+// the predecessor has completed and its writes are visible (at once when the
+// launch has no programmatic predecessor), so every memory effect keeps plain
+// stream order.  pdl_launch_dependents() lets the next launch be scheduled
+// before this one ends; it never lets the next kernel past its own pdl_wait().
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 int num_sms();  // SM count of the current device (cached)
 
 cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_t R,
@@ -197,10 +230,9 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st);
 size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);
 cudaError_t launch_gelu_table(uint16_t* table, cudaStream_t st);
-// The streaming kernel alone, on a table already built (after_table: launched
-// right behind the table kernel, as its programmatic dependent).
-cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table, bool after_table,
-                               cudaStream_t st);
+// The streaming kernel alone, on a table already built (or being built by the
+// previous launch in the stream).
+cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table, cudaStream_t st);
 // Device address and size of the library-owned activation table of the
 // current device (looked up on the first call per device).
 cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity);

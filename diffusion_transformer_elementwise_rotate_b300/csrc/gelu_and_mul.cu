@@ -44,26 +44,19 @@ __device__ __forceinline__ uint4 geglu_vec(const uint16_t* tab, uint4 g, uint4 u
     return o;
 }
 
-__device__ __forceinline__ void grid_dependents_may_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-// Blocks until the grid this launch depends on (the table kernel) has
-// completed and its writes are visible; returns at once when the launch has
-// no programmatic dependency.
-__device__ __forceinline__ void wait_for_prerequisite_grid() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 // One table entry per thread: table[i] = RN16(RN32(gelu(bf16 bits i))).
 __global__ void __launch_bounds__(256) gelu_table_kernel(uint16_t* __restrict__ table) {
-    grid_dependents_may_launch();
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel may still read this workspace
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < kTable) table[i] = gelu_entry((uint32_t)i);
 }
 
 // Copies the table from the workspace into shared memory (16 bytes per load).
 __device__ __forceinline__ void load_table(uint16_t* tab, const uint16_t* __restrict__ gtab) {
-    wait_for_prerequisite_grid();
+    pdl_launch_dependents();
+    pdl_wait();  // the table kernel (or whatever ran before) has completed
     const uint4* src = reinterpret_cast<const uint4*>(gtab);
     uint4* dst = reinterpret_cast<uint4*>(tab);
     for (int i = threadIdx.x; i < kTable / 8; i += blockDim.x) dst[i] = __ldcg(src + i);
@@ -160,11 +153,10 @@ cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity) {
 }
 
 cudaError_t launch_gelu_table(uint16_t* table, cudaStream_t st) {
-    gelu_table_kernel<<<kTable / 256, 256, 0, st>>>(table);
-    return cudaGetLastError();
+    return launch_pdl(gelu_table_kernel, dim3(kTable / 256), dim3(256), 0, st, table);
 }
 
-cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table, bool after_table,
+cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table,
                                cudaStream_t st) {
     const size_t smem = kTable * sizeof(uint16_t);
     const bool vec = (p.F % 8 == 0) && (p.s_gate % 8 == 0) && (p.s_up % 8 == 0) &&
@@ -190,31 +182,18 @@ cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table, bool
         if (e != cudaSuccess) return e;
         g_attr[dev][which].store(true, std::memory_order_release);
     }
-    // right after the table kernel, the streaming kernel is its programmatic
-    // dependent: it may start before the table kernel completes and waits for
-    // it with griddepcontrol.wait before touching the table (a no-op otherwise)
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = after_table ? 1 : 0;
-    if (vec)
-        e = cudaLaunchKernelEx(&cfg, geglu_vec_kernel<4>, p, table);
-    else
-        e = cudaLaunchKernelEx(&cfg, geglu_scalar_kernel, p, table);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    // a programmatic dependent of the table kernel (or of whatever ran before):
+    // it waits with griddepcontrol.wait before touching the table
+    return vec ? launch_pdl(geglu_vec_kernel<4>, dim3((unsigned)blocks), dim3(kThreads), smem, st,
+                            p, table)
+               : launch_pdl(geglu_scalar_kernel, dim3((unsigned)blocks), dim3(kThreads), smem, st,
+                            p, table);
 }
 
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st) {
     cudaError_t e = launch_gelu_table(table, st);
     if (e != cudaSuccess) return e;
-    return launch_gelu_stream(p, table, true, st);
+    return launch_gelu_stream(p, table, st);
 }
 
 }  // namespace dtrot

@@ -355,6 +355,8 @@ __device__ __forceinline__ void load_w(const RmsParams& p, int nv, uint4 (&wv)[V
 template <int VPT>
 __global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
     __shared__ RowShared sh;
+    pdl_launch_dependents();
+    pdl_wait();
     const int nv = (int)(p.C >> 3);
     const int tid = threadIdx.x;
     uint4 wv[VPT], xc[VPT], rc[VPT];
@@ -391,6 +393,8 @@ __global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
 // accumulates; pass 2 re-reads the thread's own h values.
 __global__ void __launch_bounds__(256) rms_generic_kernel(RmsParams p) {
     __shared__ RowShared sh;
+    pdl_launch_dependents();
+    pdl_wait();
     int slot = 0;
     for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, slot ^= 1) {
         const uint16_t* xr = p.x + row * p.sx;
@@ -438,8 +442,7 @@ cudaError_t launch_vec(const RmsParams& p, int threads, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     int64_t blocks = (int64_t)num_sms() * per_sm;
     if (blocks > p.T) blocks = p.T;
-    rms_vec_kernel<VPT><<<(unsigned)blocks, threads, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(rms_vec_kernel<VPT>, dim3((unsigned)blocks), dim3(threads), 0, st, p);
 }
 
 }  // namespace
@@ -470,8 +473,7 @@ cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st) {
     }
     int64_t blocks = p.T;
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    rms_generic_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(rms_generic_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 }  // namespace dtrot

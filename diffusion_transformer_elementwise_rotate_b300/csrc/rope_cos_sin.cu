@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) rope_cos_sin_kernel(const float* __restri
                                                           int64_t S, int64_t B, int64_t R,
                                                           uint16_t* __restrict__ cos_out,
                                                           uint16_t* __restrict__ sin_out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t groups_per_row = R / VEC;
     const int64_t total = B * S * groups_per_row;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
@@ -75,13 +77,10 @@ cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_
     const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident blocks of 256 per SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (vec)
-        rope_cos_sin_kernel<8><<<(unsigned)blocks, threads, 0, st>>>(freqs, S, B, R, cos_out,
-                                                                     sin_out);
-    else
-        rope_cos_sin_kernel<1><<<(unsigned)blocks, threads, 0, st>>>(freqs, S, B, R, cos_out,
-                                                                     sin_out);
-    return cudaGetLastError();
+    return vec ? launch_pdl(rope_cos_sin_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                            freqs, S, B, R, cos_out, sin_out)
+               : launch_pdl(rope_cos_sin_kernel<1>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                            freqs, S, B, R, cos_out, sin_out);
 }
 
 }  // namespace dtrot

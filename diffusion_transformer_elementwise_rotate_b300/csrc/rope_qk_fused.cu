@@ -85,6 +85,8 @@ template <int VW, int U, bool ANGLES>
 __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
     using V = typename QKVec<VW>::T;
     __shared__ __align__(16) uint16_t cs[kWarps][2][kMaxRot];  // angle mode: cos, sin row
+    pdl_launch_dependents();
+    pdl_wait();
     const RopeQKParams& p = a.p;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int ri = lane / a.NP;
@@ -170,6 +172,8 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
 // [0, Hq) are q's, [Hq, Hq + Hk) k's.
 template <bool ANGLES>
 __global__ void __launch_bounds__(256) rope_qk_generic_kernel(RopeQKParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t hh = p.rot >> 1;
     const int64_t rows = p.Hq + p.Hk;
     const int64_t per_tok = rows * hh;
@@ -224,8 +228,8 @@ cudaError_t launch_qk_fast(const QKArgs& a, cudaStream_t st) {
     const int64_t ntok = a.p.B * a.p.S;
     int64_t blocks = (ntok + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    rope_qk_kernel<VW, 4, ANGLES><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(rope_qk_kernel<VW, 4, ANGLES>, dim3((unsigned)blocks), dim3(kWarps * 32), 0,
+                      st, a);
 }
 
 template <bool ANGLES>
@@ -248,8 +252,7 @@ cudaError_t launch_qk(const RopeQKParams& p, cudaStream_t st) {
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    rope_qk_generic_kernel<ANGLES><<<(unsigned)blocks, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(rope_qk_generic_kernel<ANGLES>, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 }  // namespace

@@ -80,6 +80,8 @@ struct FastArgs {
 
 template <int VW, int U>
 __global__ void __launch_bounds__(256) rope_fast_kernel(FastArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
     using V = typename VecT<VW>::T;
     const RopeParams& p = a.p;
     const int lane = threadIdx.x & 31;
@@ -145,6 +147,8 @@ __global__ void __launch_bounds__(256) rope_fast_kernel(FastArgs a) {
 // Generic path: one thread per (token, head, item); item < h is the pair
 // (j, j + h), item >= h is tail column rot + (item - h).
 __global__ void __launch_bounds__(256) rope_generic_kernel(RopeParams p, int64_t items) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t hh = p.rot >> 1;
     const int64_t per_tok = p.H * items;
     const int64_t total = p.B * p.S * per_tok;
@@ -197,8 +201,7 @@ cudaError_t launch_fast(const FastArgs& a, cudaStream_t st) {
     const int64_t ntok = a.p.B * a.p.S;
     int64_t blocks = (ntok + (threads / 32) - 1) / (threads / 32);
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    rope_fast_kernel<VW, 4><<<(unsigned)blocks, threads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(rope_fast_kernel<VW, 4>, dim3((unsigned)blocks), dim3(threads), 0, st, a);
 }
 
 }  // namespace
@@ -227,8 +230,8 @@ cudaError_t launch_rope_rotate_half(const RopeParams& p, cudaStream_t st) {
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    rope_generic_kernel<<<(unsigned)blocks, threads, 0, st>>>(p, items);
-    return cudaGetLastError();
+    return launch_pdl(rope_generic_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, p,
+                      items);
 }
 
 }  // namespace dtrot
