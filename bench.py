@@ -44,6 +44,20 @@ DOM_EVERY = 8  # timed steps per step whose dominant-kernel call is bracketed by
 LAUNCHES_PER_STEP = 7
 
 
+def config_for(wl, per_step, parallelism):
+    """The `config` of both arms' lines: the workload they measure."""
+    return {
+        "workload": (f"{wl.name} DiT layer: q,k ({wl.B},{wl.S},{wl.H},{wl.D}) rot {wl.rot} "
+                     f"split {'/'.join(map(str, wl.split))}; GEGLU ({wl.T_ff}, 2x{wl.F}); "
+                     f"RMSNorm+residual ({wl.T_norm}, {wl.C}) x2; cos/sin tables "
+                     f"({wl.tokens}, {wl.rot})"),
+        "step": "tables + RoPE q + RoPE k + GEGLU + 2x RMSNorm+residual",
+        "bytes_per_step": per_step,
+        "l2": "inputs larger than L2 (126 MB) for every kernel; no flush",
+        "parallelism": parallelism,
+    }
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -572,16 +586,7 @@ def native(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/gate/up/x, N(0,4) residual, N(1,0.1) w; "
                 "rotary angles from the token grid)",
-        "config": {
-            "workload": (f"{wl.name} DiT layer: q,k ({wl.B},{wl.S},{wl.H},{wl.D}) rot {wl.rot} "
-                         f"split {'/'.join(map(str, wl.split))}; GEGLU ({wl.T_ff}, 2x{wl.F}); "
-                         f"RMSNorm+residual ({wl.T_norm}, {wl.C}) x2; cos/sin tables "
-                         f"({wl.tokens}, {wl.rot})"),
-            "step": "tables + RoPE q + RoPE k + GEGLU + 2x RMSNorm+residual",
-            "bytes_per_step": per_step,
-            "l2": "inputs larger than L2 (126 MB) for every kernel; no flush",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": config_for(wl, per_step, f"replicas x{world}"),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "mtokens_per_s_per_layer": round(tokens / (ms_per_step / 1e3) / 1e6, 3),
         "mtokens_per_s_per_layer_with_next_rows": round(
@@ -688,8 +693,7 @@ def reference(args):
         "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * el / steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 (emulated in fp64)", "data": "synthetic",
-        "config": {"workload": f"{wl.name} DiT layer (a sample of every op's rows per step)",
-                   "parallelism": "host cores"},
+        "config": config_for(wl, sum(bts.values()), "host cores"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
