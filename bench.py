@@ -588,7 +588,11 @@ def native(args):
                 "rotary angles from the token grid)",
         "config": config_for(wl, per_step, f"replicas x{world}"),
         "pct_of_peak": round(100 * value / world / peak, 2),
-        "mtokens_per_s_per_layer": round(tokens / (ms_per_step / 1e3) / 1e6, 3),
+        # B*S over the layer's ops (the tables are once per forward), per-op times
+        # from the breakdown pass; and B*S over the whole timed step
+        "mtokens_per_s_per_layer": round(
+            tokens / (sum(kern_ms[o] for o in OPS[1:]) / 1e3) / 1e6, 3),
+        "mtokens_per_s_per_step": round(tokens / (ms_per_step / 1e3) / 1e6, 3),
         "mtokens_per_s_per_layer_with_next_rows": round(
             tokens / ((fused["rope_qk_inplace_angles"]["ms"] + kern_ms["gelu_and_mul"]
                        + kern_ms["rmsnorm_residual_attn"] + kern_ms["rmsnorm_residual_ffn"])
