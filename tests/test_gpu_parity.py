@@ -629,3 +629,39 @@ def test_outputs_write_nothing_outside_their_views(pad):
     for t in (cb, sb):
         v = t.view(torch.int16)
         assert bool((v[:pad] == CANARY).all() and (v[pad + n:] == CANARY).all()), "tables"
+
+
+# ---------------------------------------------------------------- launch order
+
+def test_back_to_back_calls_keep_stream_order():
+    # Each launch may be scheduled while the previous one drains (programmatic
+    # dependent launch); every kernel waits for its predecessor before touching
+    # memory.  Queued without synchronisation: table kernels that overwrite the
+    # tables the previous RoPE call is reading, RoPE reading them right after, and
+    # RMSNorm calls chained through the residual they update in place.
+    wl = W.WORKLOADS["image"]
+    base = W.freqs_for(wl)
+    freqs = [base, base * 0.5 + 0.25, base * 2.0 - 1.0]
+    q = W.normal_bf16((wl.B, wl.S, wl.H, wl.D), 11, 0)
+    qd = to_dev(q)
+    cos = torch.empty((wl.B * wl.S, wl.rot), dtype=torch.bfloat16, device="cuda")
+    sin = torch.empty_like(cos)
+    outs = []
+    for f in freqs:
+        dt.rope_cos_sin_precompute(to_dev(f), cos, sin)
+        outs.append(dt.rope_rotate_half(qd, cos, sin))
+    T, C = 1024, 2048
+    xs = [W.normal_bf16((T, C), 12, k) for k in range(3)]
+    r = W.normal_bf16((T, C), 12, 5, std=2.0)
+    w = W.normal_bf16((C,), 12, 6, mean=1.0, std=math.sqrt(0.1))
+    rd, wd = to_dev(r.clone()), to_dev(w)
+    ys = [dt.rmsnorm_residual(to_dev(x), rd, wd, EPS) for x in xs]
+    torch.cuda.synchronize()
+    for i, f in enumerate(freqs):
+        ec, es = oracle.rope_cos_sin(f.numpy())
+        assert_bitexact(bits(outs[i]), oracle.rope_rotate_half(bits(q), ec, es), f"rope {i}")
+    h = bits(r)
+    for i, x in enumerate(xs):
+        h, y = oracle.rmsnorm_residual(bits(x), h, bits(w), EPS)
+        assert_within_tolerance(bits(ys[i]), y, f"rmsnorm {i}")
+    assert_bitexact(bits(rd), h, "residual after three calls")
