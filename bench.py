@@ -546,7 +546,7 @@ def native(args):
     ms_per_step = elapsed_ms / K
     value = aggregate_gbs(per_step, world, K, elapsed_ms)
 
-    # the next rows on the same layer: RoPE on q and k in one in-place launch,
+    # beyond the step, on the same layer: RoPE on q and k in one in-place launch,
     # with the tables or with the angles evaluated inside the kernel
     fused = fused_rope_qk(dt, layer, wl, min(K, 200))
     fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))

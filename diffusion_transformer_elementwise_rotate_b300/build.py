@@ -4,7 +4,7 @@
 
 Every .cu under csrc/ is compiled for sm_103a only and linked into one shared
 library next to this file, with the CUDA runtime linked statically so the
-library loads wherever the driver is present.
+library loads wherever the NVIDIA kernel driver is installed.
 """
 import concurrent.futures as cf
 import glob

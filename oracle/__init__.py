@@ -152,7 +152,7 @@ def gelu_bf16(xb: int) -> int:
     return int(lib().dto_gelu_bf16(int(xb)))
 
 
-# ---------------------------------------------------------------- a1
+# ---------------------------------------------------------------- cos/sin tables
 
 def rope_cos_sin(freqs: np.ndarray):
     """freqs fp32 (S, B, 1, R) -> (cos, sin), each uint16 (B*S, R)."""
@@ -175,7 +175,7 @@ def rope_cos_sin_f64(freqs: np.ndarray):
     return cos, sin
 
 
-# ---------------------------------------------------------------- a2
+# ---------------------------------------------------------------- RoPE
 
 def rope_rotate_half(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
     """x uint16 (B, S, H, D) (any element strides, last dim contiguous);
@@ -209,7 +209,7 @@ def rope_rotate_half_f64(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.
     return out
 
 
-# ---------------------------------------------------------------- a3
+# ---------------------------------------------------------------- GEGLU
 
 def gelu_and_mul(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
     """gate, up uint16 (T, F) (row strides allowed) -> out uint16 (T, F)."""
@@ -234,7 +234,7 @@ def gelu_and_mul_fused(gate_up: np.ndarray) -> np.ndarray:
     return gelu_and_mul(gate_up[:, :F], gate_up[:, F:2 * F])
 
 
-# ---------------------------------------------------------------- a4
+# ---------------------------------------------------------------- RMSNorm + residual
 
 def rmsnorm_residual(x: np.ndarray, residual: np.ndarray, w: np.ndarray, eps: float):
     """x, residual uint16 (T, C); w uint16 (C,) -> (h, y) uint16 (T, C).

@@ -87,7 +87,7 @@ EXPORT int dto_fp_env_ok(void) {
 }
 
 /* ------------------------------------------------------------------ */
-/* a1: rotary cos/sin tables (ERNIE-Image page, section 1)             */
+/* Rotary cos/sin tables (ERNIE-Image page, section 1)                 */
 /* ------------------------------------------------------------------ */
 
 /* freqs is fp32 (S, B, 1, R) contiguous; the outputs are (B*S, R) rows, row
@@ -124,7 +124,7 @@ EXPORT void dto_rope_cos_sin_f64(const double* freqs, int64_t S, int64_t B, int6
 }
 
 /* ------------------------------------------------------------------ */
-/* a2: rotate-half RoPE (ERNIE-Image page, section 2)                  */
+/* Rotate-half RoPE (ERNIE-Image page, section 2)                      */
 /* ------------------------------------------------------------------ */
 
 /* Rounding applied after each op of the eager chain: RN16 in bf16 mode, the
@@ -194,7 +194,7 @@ EXPORT void dto_rope_rotate_half_f64(const double* x, int64_t B, int64_t S, int6
 }
 
 /* ------------------------------------------------------------------ */
-/* a3: GEGLU (ERNIE-Image page, section 3)                             */
+/* GEGLU (ERNIE-Image page, section 3)                                 */
 /* ------------------------------------------------------------------ */
 
 /* gelu(x) = x * 1/2 * (1 + erf(x / sqrt 2)), the exact (erf) GELU that
@@ -226,7 +226,7 @@ EXPORT void dto_gelu_and_mul(const uint16_t* gate, int64_t s_gate, const uint16_
 }
 
 /* ------------------------------------------------------------------ */
-/* a4: RMSNorm fused with the residual add (sequence-parallelism post) */
+/* RMSNorm fused with the residual add (sequence-parallelism post)     */
 /* ------------------------------------------------------------------ */
 
 /* One token row, pre-norm order: h = R(x + r) is the new residual stream;

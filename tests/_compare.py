@@ -1,7 +1,7 @@
 """Element-wise comparison of bf16 bit arrays (numpy uint16)."""
 import numpy as np
 
-# Spec tolerance for GEGLU and RMSNorm: every element within 1 bf16 ulp,
+# Tolerance for GEGLU and RMSNorm: every element within 1 bf16 ulp,
 # and at most 0.01% of elements different at all.  RoPE and the cos/sin tables
 # must be bit-exact.
 MAX_ULP = 1

@@ -37,7 +37,7 @@ def _lib():
     torch.cuda.init()
 
 
-# ---------------------------------------------------------------- a1 tables
+# ---------------------------------------------------------------- cos/sin tables
 
 @pytest.mark.parametrize("name", ["tiny", "image", "cfg", "video"])
 def test_cos_sin_tables_bitexact(name):
@@ -95,7 +95,7 @@ def test_cos_sin_reduction_range_and_zero_crossings():
     assert_bitexact(bits(s), es, "sin")
 
 
-# ---------------------------------------------------------------- a2 RoPE
+# ---------------------------------------------------------------- RoPE
 
 def _rope_case(x, cos_b, sin_b, **kw):
     got = dt.rope_rotate_half(to_dev(x), to_dev(from_u16(cos_b)), to_dev(from_u16(sin_b)), **kw)
@@ -273,7 +273,7 @@ def test_rope_qk_video_full_size_sampled_tokens():
     assert_bitexact(bits(dk)[:, toks], oracle.rope_rotate_half(bits(k)[:, toks], ec, es), "k")
 
 
-# ---------------------------------------------------------------- a3 GEGLU
+# ---------------------------------------------------------------- GEGLU
 
 def test_geglu_every_bf16_gate_value_bitexact():
     gate = np.arange(1 << 16, dtype=np.uint16).reshape(256, 256)
@@ -384,7 +384,7 @@ def test_geglu_empty():
     assert dt.gelu_and_mul(z, z).shape == (0, 16)
 
 
-# ---------------------------------------------------------------- a4 RMSNorm
+# ---------------------------------------------------------------- RMSNorm
 
 def _rms_check(x, r, w, rows=None, what="", exact=True):
     xd, rd, wd = to_dev(x), to_dev(r), to_dev(w)
