@@ -15,6 +15,10 @@
  *    default stream.  Work is enqueued on it and the call returns without
  *    synchronising.  The library allocates nothing, frees nothing and makes no
  *    host-device synchronisation, so calls may be captured in a CUDA graph.
+ *  - Each kernel is launched as a programmatic dependent of the work before it
+ *    in the stream (so its launch overlaps the end of that work) and waits for
+ *    that work to complete before it reads or writes any memory: the memory
+ *    effects of the calls keep plain stream order.
  *  - The caller owns every buffer.  Outputs are fully overwritten; inputs are
  *    only read, except `residual` of dtrot_rmsnorm_residual, which is updated.
  *  - Any alignment is accepted.  Pointers and strides that are multiples of
@@ -230,11 +234,15 @@ int64_t dtrot_gemm_gelu_and_mul_workspace_bytes(void);
  *             16-byte aligned (else DTROT_ERR_WORKSPACE), owned by the caller,
  *             contents on entry ignored: the call writes its activation table
  *             there (bytes [0, 17152)) and an error word (bytes [17152, 17156),
- *             zero unless a wait inside the kernel ran out of time, which
- *             would mean the GPU stopped making progress).  Calls that may run
- *             at the same time on the GPU must use different workspaces.
+ *             zero unless a wait inside the kernel ran out of time (bits 1, 2,
+ *             4) or the two CTAs of a pair were given different tensor-memory
+ *             columns (bit 8); either would mean the GPU misbehaved, and the
+ *             output is then not valid).  Calls that may run at the same time
+ *             on the GPU must use different workspaces.
  * Two kernels are enqueued on `stream`: the activation table, then the GEMM
- * as its programmatic dependent.  Needs an sm_103 GPU (tcgen05 tensor cores).
+ * as its programmatic dependent.  For T > 128 the GEMM runs on pairs of CTAs
+ * (clusters of two, tcgen05 cta_group::2 MMAs on 256-row tiles); for smaller T
+ * on single CTAs.  Needs an sm_103 GPU (tcgen05 tensor cores).
  */
 dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int64_t C, const uint16_t* w,
                                      int64_t F, uint16_t* out, int64_t s_out, uint16_t* gate_up,
