@@ -1,7 +1,6 @@
 // extern "C" entry points of libdtrot: host-side argument validation, then one
 // kernel launch on the caller's stream.  The declarations, with the meaning,
 // layout, ownership and error behaviour of every argument, are in dtrot.h.
-#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -75,11 +74,18 @@ bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi
 
 // True if no two distinct index tuples of the view share an element.
 bool non_self_overlapping(const int64_t* size, const int64_t* stride, int n) {
-    int idx[8];
+    constexpr int kMaxDims = 8;
+    if (n < 0 || n > kMaxDims) return false;
+    int idx[kMaxDims];
     int m = 0;
     for (int i = 0; i < n; ++i)
         if (size[i] > 1) idx[m++] = i;
-    std::sort(idx, idx + m, [&](int a, int b) { return stride[a] < stride[b]; });
+    for (int k = 1; k < m; ++k) {  // insertion sort by stride (m <= 8)
+        const int v = idx[k];
+        int j = k;
+        for (; j > 0 && stride[idx[j - 1]] > stride[v]; --j) idx[j] = idx[j - 1];
+        idx[j] = v;
+    }
     int64_t extent = 0;  // elements spanned by the dims already placed, minus one
     for (int k = 0; k < m; ++k) {
         const int i = idx[k];
