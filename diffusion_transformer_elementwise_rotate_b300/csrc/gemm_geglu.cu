@@ -21,8 +21,9 @@
 //   - epilogue: each of 4 warps reads its 32 accumulator lanes (rows) with
 //     tcgen05.ld, rounds gate and up to bf16 (the projection's output
 //     rounding), looks the activation up in a compact 17 KB table in shared
-//     memory and multiplies with one bf16x2 .rn multiply, as the standalone
-//     GEGLU kernel does;
+//     memory, multiplies with one bf16x2 .rn multiply, as the standalone GEGLU
+//     kernel does, and stores 32 x 32 output blocks through shared memory
+//     with TMA;
 //   - optionally the rounded gate and up are stored too (a (T, 2F) gate_up
 //     tensor, for a backward pass or for checking);
 //   - tiles are visited in groups of row tiles so that the x and W tiles a
@@ -38,7 +39,8 @@
 //       two fits.
 // Every mbarrier wait is bounded (about a second of %globaltimer): a wait that
 // runs out records a code in the workspace's error word and the CTA finishes
-// without further waits; later CTAs that see the word set exit at once.
+// without further waits (single CTAs that start later and see the word set
+// exit at once; the pair kernel's clusters all start together).
 #include <cuda.h>
 
 #include <atomic>
