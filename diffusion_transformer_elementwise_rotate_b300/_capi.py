@@ -50,6 +50,10 @@ SIGNATURES = {
     "dtrot_gemm_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
     "dtrot_gemm_gelu_and_mul": (ctypes.c_int, [_p, _i64, _i64, _p, _i64, _p, _i64, _p, _i64,
                                                _p, _i64, _p]),
+    "dtrot_gemm_gelu_and_mul_withhold_last_stage": (ctypes.c_int, [_p, _i64, _i64, _p, _i64, _p,
+                                                                   _i64, _p, _i64, _p, _i64,
+                                                                   _p]),
+    "dtrot_gemm_gelu_and_mul_error": (ctypes.c_int, [_p, _p, _p]),
     "dtrot_gelu_and_mul_noalloc": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p]),
     "dtrot_rmsnorm_residual": (ctypes.c_int,
                                [_p, _i64, _p, _i64, _p, ctypes.c_float, _p, _i64, _i64, _i64,
@@ -59,6 +63,11 @@ SIGNATURES = {
 
 class DtrotUnavailable(RuntimeError):
     pass
+
+
+class DtrotKernelError(RuntimeError):
+    """A kernel reported a failure through its error word (its output is not
+    valid)."""
 
 
 class DtrotError(RuntimeError):

@@ -12,8 +12,11 @@ runs in libdtrot's sm_103a kernels.
   gelu_and_mul(gate, up, out=None, workspace=None, table=None) -> out   ERNIE-Image page, section 3
   gelu_table(device)                      -> the activation table, built once per device
   gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
-  gemm_gelu_and_mul(x, w, out=None, workspace=None) -> out   GEGLU in the epilogue of the
-                                         gate_up projection x w^T (tcgen05 tensor cores)
+  gemm_gelu_and_mul(x, w, out=None, workspace=None, check=False) -> out   GEGLU in the
+                                         epilogue of the gate_up projection x w^T (tcgen05
+                                         tensor cores); check=True reads the kernel's
+                                         error word and raises on a failure
+  gemm_error_word(workspace)              -> the error word of the last call on it
   rmsnorm_residual(x, residual, w, eps=1e-6, out=None) -> out   (residual updated in place)
                                                          sequence-parallelism post
 """
@@ -257,13 +260,32 @@ def _cached_workspace(kind: str, query: str, device: torch.device, stream: int) 
     return ws
 
 
+def gemm_error_word(workspace: torch.Tensor) -> int:
+    """The error word a gemm_gelu_and_mul call left in `workspace` (0: every
+    wait completed and the output is valid; see dtrot_gemm_gelu_and_mul_error).
+    Reads it on the current stream, after the calls queued there, and waits
+    for that read."""
+    import ctypes
+    word = ctypes.c_uint32(0)
+    st = torch.cuda.current_stream(workspace.device)
+    _capi.check("dtrot_gemm_gelu_and_mul_error", workspace.data_ptr(), ctypes.addressof(word),
+                st.cuda_stream)
+    st.synchronize()
+    return int(word.value)
+
+
 def gemm_gelu_and_mul(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
                       workspace: torch.Tensor | None = None,
-                      gate_up: torch.Tensor | None = None) -> torch.Tensor:
+                      gate_up: torch.Tensor | None = None, check: bool = False,
+                      _withhold_last_stage: bool = False) -> torch.Tensor:
     """GEGLU of the MLP's gate_up projection without storing gate_up:
     x bf16 (T, C), w bf16 (2F, C) (gate rows first) -> out bf16 (T, F) =
     up * gelu(gate) with gate_up = x w^T rounded to bf16.  If `gate_up` (bf16
-    (T, 2F)) is given, the rounded projection is stored there as well."""
+    (T, 2F)) is given, the rounded projection is stored there as well.
+    With check=True the call waits for the kernel and raises DtrotKernelError
+    if it reported a failure in its error word (a wait that ran out of time);
+    `_withhold_last_stage` runs the diagnostic variant whose last pipeline
+    stage is never loaded (tests only)."""
     _need(x, "x", torch.bfloat16)
     _need(w, "w", torch.bfloat16)
     if x.dim() != 2 or w.dim() != 2 or w.shape[1] != x.shape[1] or w.shape[0] % 2:
@@ -289,9 +311,18 @@ def gemm_gelu_and_mul(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None
             raise ValueError("gate_up must be (T, 2F)")
         gp, sgu = gate_up.data_ptr(), _rows(gate_up, "gate_up")
     key = _sc.want("gemm_gelu_and_mul", x, w)
-    _capi.check("dtrot_gemm_gelu_and_mul", x.data_ptr(), T, C, w.data_ptr(), F, out.data_ptr(),
+    entry = ("dtrot_gemm_gelu_and_mul_withhold_last_stage" if _withhold_last_stage
+             else "dtrot_gemm_gelu_and_mul")
+    _capi.check(entry, x.data_ptr(), T, C, w.data_ptr(), F, out.data_ptr(),
                 so, gp or None, sgu, workspace.data_ptr(),
                 workspace.numel() * workspace.element_size(), st)
+    if check:
+        word = gemm_error_word(workspace)
+        if word:
+            raise _capi.DtrotKernelError(
+                f"gemm_gelu_and_mul: the kernel reported error word {word:#x} "
+                "(1: free stage, 2: loaded stage, 4: accumulator wait ran out of time; "
+                "8: CTA pair tensor-memory mismatch); its output is not valid")
     if key:
         def rerun(rows):
             o = torch.empty((rows, F), dtype=torch.bfloat16, device=x.device)

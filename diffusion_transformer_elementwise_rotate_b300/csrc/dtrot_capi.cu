@@ -1,6 +1,8 @@
 // extern "C" entry points of libdtrot: host-side argument validation, then one
 // kernel launch on the caller's stream.  The declarations, with the meaning,
 // layout, ownership and error behaviour of every argument, are in dtrot.h.
+#include <cuda.h>
+
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -151,6 +153,42 @@ dtrot_status launch_status(cudaError_t e) {
 }
 
 }  // namespace
+
+uint64_t current_context_id() {
+    // cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points
+    // (no link-time dependency on libcuda)
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static std::atomic<GetCurrent> s_cur{nullptr};
+    static std::atomic<GetId> s_id{nullptr};
+    static std::atomic<int> s_missing{0};
+    if (s_missing.load(std::memory_order_relaxed)) return 0;
+    GetCurrent cur = s_cur.load(std::memory_order_acquire);
+    GetId gid = s_id.load(std::memory_order_acquire);
+    if (!cur || !gid) {
+        void* p1 = nullptr;
+        void* p2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || !p1 ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) !=
+                cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess || !p2) {
+            s_missing.store(1, std::memory_order_relaxed);
+            return 0;
+        }
+        cur = reinterpret_cast<GetCurrent>(p1);
+        gid = reinterpret_cast<GetId>(p2);
+        s_cur.store(cur, std::memory_order_release);
+        s_id.store(gid, std::memory_order_release);
+    }
+    CUcontext ctx = nullptr;
+    if (cur(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (gid(ctx, &id) != CUDA_SUCCESS) return 0;
+    return (uint64_t)id;
+}
 
 int num_sms() {
     const int dev = current_device();
@@ -435,7 +473,10 @@ DTROT_API dtrot_status dtrot_gelu_and_mul_with_table(const uint16_t* gate, int64
 
 // GEGLU for callers that cannot allocate device memory: the same computation
 // as dtrot_gelu_and_mul, with the activation table kept in the library's own
-// static device array instead of a caller workspace.
+// static device array instead of a caller workspace.  Every argument is
+// checked, in the order dtrot_gelu_and_mul checks them, before the device is
+// queried or the array's address looked up, so the two entry points return
+// the same status for the same invalid call.
 DTROT_API dtrot_status dtrot_gelu_and_mul_noalloc(const uint16_t* gate, int64_t s_gate,
                                                   const uint16_t* up, int64_t s_up, uint16_t* out,
                                                   int64_t s_out, int64_t T, int64_t F,
@@ -445,29 +486,40 @@ DTROT_API dtrot_status dtrot_gelu_and_mul_noalloc(const uint16_t* gate, int64_t 
     if (!mul_ok(T, F, &n) || !mul_ok(n, 8, &n)) return DTROT_ERR_SHAPE;
     if (n == 0) return DTROT_OK;
     if (!gate || !up || !out) return DTROT_ERR_NULL;
+    GegluParams p;
+    const dtrot_status v = geglu_views(gate, s_gate, up, s_up, out, s_out, T, F, &p);
+    if (v != DTROT_OK) return v;
     if (!device_ok()) return DTROT_ERR_DEVICE;
     uint16_t* table = nullptr;
     size_t capacity = 0;
+    const cudaError_t pending = cudaPeekAtLastError();
     if (noalloc_gelu_table(&table, &capacity) != cudaSuccess) {
-        cudaGetLastError();
+        // clear the lookup's own error, but leave an error the caller already
+        // had pending in place
+        if (pending == cudaSuccess) cudaGetLastError();
         return DTROT_ERR_DEVICE;
     }
     // the table's size is fixed (it does not grow with T or F); a library
     // whose table outgrew the static array would refuse every call here
     if (gelu_table_bytes() > capacity) return DTROT_ERR_WORKSPACE;
-    return dtrot_gelu_and_mul(gate, s_gate, up, s_up, out, s_out, T, F, table,
-                              (int64_t)capacity, stream);
+    const int64_t wb = (int64_t)gelu_table_bytes();
+    if (!range_disjoint(table, wb, gate, p.s_gate, T, F) ||
+        !range_disjoint(table, wb, up, p.s_up, T, F) ||
+        !range_disjoint(table, wb, out, p.s_out, T, F))
+        return DTROT_ERR_ALIAS;
+    return launch_status(launch_gelu_and_mul(p, table, (cudaStream_t)stream));
 }
 
 DTROT_API int64_t dtrot_gemm_gelu_and_mul_workspace_bytes(void) {
     return (int64_t)gemm_geglu_workspace_bytes();
 }
 
-DTROT_API dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int64_t C,
-                                               const uint16_t* w, int64_t F, uint16_t* out,
-                                               int64_t s_out, uint16_t* gate_up,
-                                               int64_t s_gate_up, void* workspace,
-                                               int64_t workspace_bytes, void* stream) {
+// Validation and launch of the projection with GEGLU in its epilogue;
+// `withhold` selects the diagnostic run whose last pipeline stage is withheld.
+static dtrot_status gemm_call(const uint16_t* x, int64_t T, int64_t C, const uint16_t* w,
+                              int64_t F, uint16_t* out, int64_t s_out, uint16_t* gate_up,
+                              int64_t s_gate_up, void* workspace, int64_t workspace_bytes,
+                              void* stream, int withhold) {
     if (T < 0 || C < 0 || F < 0) return DTROT_ERR_SHAPE;
     int64_t n, f2, nw;
     if (!mul_ok(T, C, &n) || !mul_ok(n, 2, &n) || !mul_ok(F, 2, &f2) || !mul_ok(f2, C, &nw) ||
@@ -516,7 +568,35 @@ DTROT_API dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int
     a.gate_up = gate_up;
     a.s_gate_up = sg;
     a.workspace = workspace;
+    a.withhold_last_stage = withhold;
     return launch_status(launch_gemm_geglu(a, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int64_t C,
+                                               const uint16_t* w, int64_t F, uint16_t* out,
+                                               int64_t s_out, uint16_t* gate_up,
+                                               int64_t s_gate_up, void* workspace,
+                                               int64_t workspace_bytes, void* stream) {
+    return gemm_call(x, T, C, w, F, out, s_out, gate_up, s_gate_up, workspace, workspace_bytes,
+                     stream, 0);
+}
+
+DTROT_API dtrot_status dtrot_gemm_gelu_and_mul_withhold_last_stage(
+    const uint16_t* x, int64_t T, int64_t C, const uint16_t* w, int64_t F, uint16_t* out,
+    int64_t s_out, uint16_t* gate_up, int64_t s_gate_up, void* workspace,
+    int64_t workspace_bytes, void* stream) {
+    return gemm_call(x, T, C, w, F, out, s_out, gate_up, s_gate_up, workspace, workspace_bytes,
+                     stream, 1);
+}
+
+DTROT_API dtrot_status dtrot_gemm_gelu_and_mul_error(const void* workspace, uint32_t* host_word,
+                                                     void* stream) {
+    if (!workspace || !host_word) return DTROT_ERR_NULL;
+    if ((uintptr_t)workspace % 16) return DTROT_ERR_WORKSPACE;
+    if (!device_ok()) return DTROT_ERR_DEVICE;
+    const uint8_t* src = static_cast<const uint8_t*>(workspace) + gemm_geglu_error_offset();
+    return launch_status(cudaMemcpyAsync(host_word, src, sizeof(uint32_t),
+                                         cudaMemcpyDeviceToHost, (cudaStream_t)stream));
 }
 
 DTROT_API dtrot_status dtrot_rmsnorm_residual(const uint16_t* x, int64_t sx, uint16_t* residual,

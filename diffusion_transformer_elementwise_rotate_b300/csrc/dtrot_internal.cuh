@@ -168,6 +168,7 @@ struct GemmGegluArgs {
     uint16_t* gate_up;   // optional (T, 2F), row stride s_gate_up
     int64_t s_gate_up;
     void* workspace;     // gemm_geglu_workspace_bytes()
+    int withhold_last_stage = 0;  // diagnostic (see dtrot_gemm_gelu_and_mul_withhold_last_stage)
 };
 
 struct GegluParams {
@@ -220,12 +221,18 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 int num_sms();  // SM count of the current device (cached)
+// Process-unique id of the CUDA context current on this thread (cuCtxGetId),
+// 0 if none is current.  Per-device set-up (function attributes, symbol
+// addresses) is cached against it, so it is redone after cudaDeviceReset
+// gives the device a new primary context.
+uint64_t current_context_id();
 
 cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_t R,
                                 uint16_t* cos_out, uint16_t* sin_out, cudaStream_t st);
 cudaError_t launch_rope_rotate_half(const RopeParams& p, cudaStream_t st);
 cudaError_t launch_rope_qk(const RopeQKParams& p, cudaStream_t st);
 size_t gemm_geglu_workspace_bytes();
+size_t gemm_geglu_error_offset();  // byte offset of the error word in that workspace
 cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st);
 size_t gelu_table_bytes();  // workspace the GEGLU launch needs for its activation table
 cudaError_t launch_gelu_and_mul(const GegluParams& p, uint16_t* table, cudaStream_t st);

@@ -20,6 +20,7 @@
 // Table entries: gelu_entry (shared with the GEGLU epilogue of the gate_up
 // projection).
 #include <atomic>
+#include <mutex>
 
 #include "dtrot_internal.cuh"
 
@@ -119,7 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1) geglu_scalar_kernel(GegluParams p
 bool aligned(const void* ptr, int bytes) { return ((uintptr_t)ptr % bytes) == 0; }
 
 constexpr int kMaxDev = 64;
-std::atomic<bool> g_attr[kMaxDev][2];  // dynamic shared memory attribute set, per device
+// context (current_context_id) for which the dynamic shared memory attribute
+// was set, per device and kernel; 0: not yet
+std::atomic<uint64_t> g_attr_ctx[kMaxDev][2];
 
 // Activation table owned by the library, for callers that cannot hand in a
 // workspace (dtrot_gelu_and_mul_noalloc).  One copy per device that loads the
@@ -127,7 +130,16 @@ std::atomic<bool> g_attr[kMaxDev][2];  // dynamic shared memory attribute set, p
 // name as a device address: it is a host-side stand-in, and its device address
 // comes from cudaGetSymbolAddress.
 static __device__ __align__(256) uint16_t g_noalloc_table[kTable];
-std::atomic<uintptr_t> g_noalloc_addr[kMaxDev];  // device address, once per device
+
+// Its device address per device, with the context it was looked up in: a new
+// context (cudaDeviceReset, then any CUDA call) loads the library's device
+// code again, and the array may then sit at another address.
+struct NoallocSlot {
+    uint64_t ctx;
+    uintptr_t addr;
+};
+std::mutex g_noalloc_mu;
+NoallocSlot g_noalloc[kMaxDev];
 
 }  // namespace
 
@@ -138,16 +150,19 @@ cudaError_t noalloc_gelu_table(uint16_t** table, size_t* capacity) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    uintptr_t a = g_noalloc_addr[dev].load(std::memory_order_acquire);
-    if (a == 0) {
-        // first use on this device (which is current): look up the address
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    const uint64_t ctx = current_context_id();
+    NoallocSlot& slot = g_noalloc[dev];
+    if (ctx == 0 || slot.ctx != ctx || slot.addr == 0) {
+        // first use on this device in this context (the device is current):
+        // look the address up; this also creates the context if none exists
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_table);
         if (e != cudaSuccess) return e;
-        a = (uintptr_t)ptr;
-        g_noalloc_addr[dev].store(a, std::memory_order_release);
+        slot.addr = (uintptr_t)ptr;
+        slot.ctx = current_context_id();
     }
-    *table = reinterpret_cast<uint16_t*>(a);
+    *table = reinterpret_cast<uint16_t*>(slot.addr);
     *capacity = sizeof(g_noalloc_table);
     return cudaSuccess;
 }
@@ -174,13 +189,14 @@ cudaError_t launch_gelu_stream(const GegluParams& p, const uint16_t* table,
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     const int which = vec ? 0 : 1;
-    if (!g_attr[dev][which].load(std::memory_order_acquire)) {
+    const uint64_t ctx = current_context_id();
+    if (ctx == 0 || g_attr_ctx[dev][which].load(std::memory_order_acquire) != ctx) {
         e = vec ? cudaFuncSetAttribute(geglu_vec_kernel<4>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                 : cudaFuncSetAttribute(geglu_scalar_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        g_attr[dev][which].store(true, std::memory_order_release);
+        g_attr_ctx[dev][which].store(current_context_id(), std::memory_order_release);
     }
     // a programmatic dependent of the table kernel (or of whatever ran before):
     // it waits with griddepcontrol.wait before touching the table

@@ -102,6 +102,9 @@ struct GemmGegluParams {
     const uint16_t* table;  // compact activation table in the workspace
     uint32_t* err;          // error word in the workspace
     int num_m, num_n;
+    // diagnostic: when set, each producer withholds the loads of its last
+    // stage use, so the MMA thread's bounded wait for that stage runs out
+    int withhold_last_stage;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -552,7 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < tiles && !s_abort; t += gridDim.x) {
                 int m0, f0;
                 tile_coords<BM, kGroupM>(t, p.num_m, p.num_n, m0, f0);
+                const bool last_tile = t + (int)gridDim.x >= tiles;
                 for (int kb = 0; kb < nk; ++kb) {
+                    if (p.withhold_last_stage && last_tile && kb == nk - 1) break;
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (it >= (uint32_t)kStages &&
@@ -743,7 +748,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tile_coords<2 * BM, kGroupMP>(t, p.num_m, p.num_n, m0, f0);
                 const int32_t xrow = m0 + (int32_t)rank * BM;
                 const int32_t wrow = (rank ? (int32_t)p.F : 0) + f0;
+                const bool last_tile = t + clusters >= tiles;
                 for (int kb = 0; kb < nk; ++kb) {
+                    // both CTAs of the pair withhold the same stage use
+                    if (p.withhold_last_stage && last_tile && kb == nk - 1) break;
                     const uint32_t s = it % kStagesP;
                     const uint32_t ph = (it / kStagesP) & 1u;
                     if (it >= (uint32_t)kStagesP &&
@@ -845,7 +853,8 @@ constexpr size_t kSmemBytesP = 1024 + (size_t)kStagesP * kStageBytesP + kOutStag
 static_assert(kSmemBytes <= 232448 && kSmemBytesP <= 232448, "shared memory per CTA");
 
 constexpr int kMaxDev = 64;
-std::atomic<bool> g_smem_attr[kMaxDev];
+// context (current_context_id) for which the shared memory attributes were set
+std::atomic<uint64_t> g_smem_attr_ctx[kMaxDev];
 // per device: co-resident clusters of the pair kernel + 1 (0: not asked yet)
 std::atomic<int> g_pair_clusters[kMaxDev];
 
@@ -921,20 +930,22 @@ cudaError_t pair_clusters(int dev, int* out) {
 }  // namespace
 
 size_t gemm_geglu_workspace_bytes() { return kWorkspaceBytes; }
+size_t gemm_geglu_error_offset() { return kErrOffset; }
 
 cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    if (!g_smem_attr[dev].load(std::memory_order_acquire)) {
+    const uint64_t ctx = current_context_id();
+    if (ctx == 0 || g_smem_attr_ctx[dev].load(std::memory_order_acquire) != ctx) {
         e = cudaFuncSetAttribute(gemm_geglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(gemm_geglu_pair_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
         if (e != cudaSuccess) return e;
-        g_smem_attr[dev].store(true, std::memory_order_release);
+        g_smem_attr_ctx[dev].store(current_context_id(), std::memory_order_release);
     }
     CUtensorMap mx, mw, mo;
     if (!make_map(&mx, a.x, a.T, a.C) || !make_map(&mw, a.w, 2 * a.F, a.C) ||
@@ -958,6 +969,7 @@ cudaError_t launch_gemm_geglu(const GemmGegluArgs& a, cudaStream_t st) {
     p.table = table;
     p.err = err;
     p.num_n = (int)((a.F + BNH - 1) / BNH);
+    p.withhold_last_stage = a.withhold_last_stage;
 
     // CTA pairs unless a pair tile would be half empty or no cluster fits
     int clusters = 0;

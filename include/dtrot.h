@@ -250,20 +250,67 @@ dtrot_status dtrot_gemm_gelu_and_mul(const uint16_t* x, int64_t T, int64_t C, co
                                      void* stream);
 
 /*
+ * The error word of a dtrot_gemm_gelu_and_mul call.     [P4] "why this is good",
+ *                                                         item 2 (a fused path
+ *                                                         whose failure is
+ *                                                         detected, not silent)
+ *
+ * Enqueues on `stream` one copy of the 4-byte error word from `workspace`
+ * (the workspace of an earlier call on the same stream) into *host_word.  The
+ * word is there once the stream has reached the copy (cudaStreamSynchronize;
+ * with pageable host memory the copy has completed when this returns).  0
+ * means every wait of that call completed and the output is valid; otherwise
+ * bit 1, 2 or 4 says a wait for a free stage, a loaded stage or an
+ * accumulator ran out of time (about a second each, after which the kernel
+ * stops waiting, drains what it issued, frees its tensor memory and returns),
+ * and bit 8 that the two CTAs of a pair were given different tensor-memory
+ * columns; the output of that call is then not valid.  Each call clears the
+ * word before its GEMM starts, so it reports the last call on the workspace.
+ *   workspace  as passed to dtrot_gemm_gelu_and_mul (NULL: DTROT_ERR_NULL; not
+ *              16-byte aligned: DTROT_ERR_WORKSPACE).
+ *   host_word  host memory, written (NULL: DTROT_ERR_NULL).
+ * A failed copy returns DTROT_ERR_LAUNCH.
+ */
+dtrot_status dtrot_gemm_gelu_and_mul_error(const void* workspace, uint32_t* host_word,
+                                           void* stream);
+
+/*
+ * Diagnostic run of dtrot_gemm_gelu_and_mul: the same arguments, validation
+ * and launch, except that the TMA producer of every CTA (of both CTAs of a
+ * pair) withholds the loads of its last pipeline stage, so the MMA thread's
+ * bounded wait for that stage runs out after about a second.  The kernel
+ * then records bit 2 in the error word, drains what it issued, frees its
+ * tensor memory and returns; the output is not valid.  It exists to check,
+ * on a real GPU, that a stalled pipeline is reported through
+ * dtrot_gemm_gelu_and_mul_error instead of hanging the device; nothing on
+ * the hot path calls it.
+ */
+dtrot_status dtrot_gemm_gelu_and_mul_withhold_last_stage(
+    const uint16_t* x, int64_t T, int64_t C, const uint16_t* w, int64_t F, uint16_t* out,
+    int64_t s_out, uint16_t* gate_up, int64_t s_gate_up, void* workspace,
+    int64_t workspace_bytes, void* stream);
+
+/*
  * GEGLU that allocates nothing and needs no workspace.  The paper has no
  * counterpart to this entry point; it is an addition of this library.
  *
  * Same arguments, result and error codes as dtrot_gelu_and_mul, without the
- * workspace.  For callers that cannot obtain device memory of their own: for
- * example code embedded in a host framework that plans every device
- * allocation ahead and hands the code only its input and output tensors (an
- * extra cudaMalloc would break the framework's memory budget or is not
- * permitted there), or a plain C caller that has no allocator to draw from.  The 128 KB activation table lives in a static device
- * array inside this library instead; every GPU that loads the library holds
- * one such array until the process exits.
+ * workspace (every argument is checked before the device is queried, so an
+ * invalid call returns the same status from both).  For callers that cannot
+ * obtain device memory of their own: for example code embedded in a host
+ * framework that plans every device allocation ahead and hands the code only
+ * its input and output tensors (an extra cudaMalloc would break the
+ * framework's memory budget or is not permitted there), or a plain C caller
+ * that has no allocator to draw from.  The 128 KB activation table lives in a
+ * static device array inside this library instead; every GPU that loads the
+ * library holds one such array until the process exits.
  *   - The first call on a device looks up that array's device address
- *     (cudaGetSymbolAddress, with the device current) and caches it; make that
- *     first call before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with the device current) and caches it with the
+ *     device's current context; make that first call before any stream
+ *     capture on the device.  After cudaDeviceReset the device gets a new
+ *     context, in which the array may lie elsewhere: the next call sees the
+ *     new context and looks the address up again (so that call, too, should
+ *     come before any stream capture).
  *   - The table's size does not depend on T or F, so no valid size is too big
  *     for the array; if a library build's table ever exceeded the array, every
  *     call would return DTROT_ERR_WORKSPACE.  T and F are limited as for

@@ -45,7 +45,9 @@ def test_header_declares_the_four_ops():
                "dtrot_rope_rotate_half_qk", "dtrot_gelu_and_mul",
                "dtrot_gelu_and_mul_workspace_bytes", "dtrot_gelu_table_build",
                "dtrot_gelu_and_mul_with_table", "dtrot_gemm_gelu_and_mul",
-               "dtrot_gemm_gelu_and_mul_workspace_bytes", "dtrot_rmsnorm_residual",
+               "dtrot_gemm_gelu_and_mul_workspace_bytes", "dtrot_gemm_gelu_and_mul_error",
+               "dtrot_gemm_gelu_and_mul_withhold_last_stage", "dtrot_gelu_and_mul_noalloc",
+               "dtrot_rmsnorm_residual",
                "dtrot_status_str", "dtrot_version"):
         assert op in names
 
@@ -176,6 +178,23 @@ def test_gemm_gelu_and_mul_validation(lib):
 def test_gemm_gelu_and_mul_valid_call_reaches_device_check(lib):
     assert gemm() == _capi.ERR_DEVICE
     assert gemm(gu=W) == _capi.ERR_DEVICE
+    assert _capi.call("dtrot_gemm_gelu_and_mul_withhold_last_stage", P, 4, 64, Q, 16, R, 16,
+                      None, 32, WS, 17408, None) == _capi.ERR_DEVICE
+    word = ctypes.c_uint32(0)
+    assert _capi.call("dtrot_gemm_gelu_and_mul_error", WS, ctypes.addressof(word),
+                      None) == _capi.ERR_DEVICE
+
+
+def test_gemm_error_word_read_validation(lib):
+    word = ctypes.c_uint32(0)
+    assert _capi.call("dtrot_gemm_gelu_and_mul_error", None, ctypes.addressof(word),
+                      None) == _capi.ERR_NULL
+    assert _capi.call("dtrot_gemm_gelu_and_mul_error", WS, None, None) == _capi.ERR_NULL
+    assert _capi.call("dtrot_gemm_gelu_and_mul_error", WS + 4, ctypes.addressof(word),
+                      None) == _capi.ERR_WORKSPACE
+    # the diagnostic run validates like the plain call
+    assert _capi.call("dtrot_gemm_gelu_and_mul_withhold_last_stage", P, 4, 60, Q, 16, R, 16,
+                      None, 32, WS, 17408, None) == _capi.ERR_ALIGN
 
 
 def test_zero_sized_calls_are_noops(lib):
@@ -327,3 +346,31 @@ def test_missing_library_fails_loudly(tmp_path):
             _capi.load(str(tmp_path / "missing.so"))
     finally:
         _capi._lib = saved
+
+
+def geglu_noalloc(**kw):
+    a = dict(gate=P, sg=16, up=P + 16, su=16, out=W, so=8, T=4, F=8)
+    a.update(kw)
+    return _capi.call("dtrot_gelu_and_mul_noalloc", a["gate"], a["sg"], a["up"], a["su"],
+                      a["out"], a["so"], a["T"], a["F"], None)
+
+
+def test_noalloc_gelu_and_mul_rejects_what_the_workspace_entry_point_rejects(lib):
+    # every invalid call returns its status before the device is queried, and
+    # the same status as dtrot_gelu_and_mul with a valid workspace
+    cases = [dict(T=-1), dict(F=-8), dict(T=1 << 62, F=4), dict(gate=0), dict(up=0),
+             dict(out=0), dict(sg=4), dict(su=7), dict(so=7), dict(sg=-16),
+             dict(out=P + 16, so=16), dict(out=P + 8, so=16), dict(out=P, so=8)]
+    for kw in cases:
+        want = geglu(**kw)
+        assert want not in (_capi.OK, _capi.ERR_DEVICE), kw
+        assert geglu_noalloc(**kw) == want, kw
+    assert geglu_noalloc(T=0, gate=0, up=0, out=0) == _capi.OK
+    assert geglu_noalloc(F=0) == _capi.OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host without a GPU only")
+@no_device
+def test_noalloc_gelu_and_mul_valid_call_reaches_device_check(lib):
+    assert geglu_noalloc() == _capi.ERR_DEVICE
+    assert geglu_noalloc(out=P, so=16) == _capi.ERR_DEVICE   # in place

@@ -158,3 +158,33 @@ def test_strided_output_and_caller_workspace():
     assert_bitexact(bits(out), oracle.gemm_gelu_and_mul(bits(x), bits(w)), "strided out")
     assert (big[:, :8] == 7.0).all() and (big[:, 8 + F:] == 7.0).all()
     assert int(ws[17152:17156].view(torch.int32).item()) == 0
+
+
+# A stalled pipeline: the diagnostic entry point withholds the loads of each
+# CTA's last stage, so the MMA thread's bounded wait for that stage runs out
+# (about a second; nothing ever loads it).  The kernel must come back on its
+# own with bit 2 (a loaded-stage wait ran out) in its error word, the API must
+# raise when asked to check, and the next call on the same workspace must be
+# clean and exact: the device stays usable.  T = 100 runs single CTAs, T = 512
+# CTA pairs.
+@pytest.mark.parametrize("T,C,F", [(100, 256, 128), (512, 256, 256)])
+def test_stalled_pipeline_is_reported_and_the_device_stays_usable(T, C, F):
+    import time
+    x = _grid_values((T, C), 11).cuda()
+    w = _grid_values((2 * F, C), 12).cuda()
+    n = int(_capi.load().dtrot_gemm_gelu_and_mul_workspace_bytes())
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, F), dtype=torch.bfloat16, device="cuda")
+    t0 = time.time()
+    dt.gemm_gelu_and_mul(x, w, out=out, workspace=ws, _withhold_last_stage=True)
+    word = dt.api.gemm_error_word(ws)
+    elapsed = time.time() - t0
+    assert word & 2, f"error word {word:#x}: the withheld stage's wait did not report"
+    assert word & ~0x7 == 0, f"error word {word:#x}"
+    assert elapsed < 30.0
+    with pytest.raises(_capi.DtrotKernelError):
+        dt.gemm_gelu_and_mul(x, w, out=out, workspace=ws, check=True, _withhold_last_stage=True)
+    got = dt.gemm_gelu_and_mul(x, w, out=out, workspace=ws, check=True)
+    assert dt.api.gemm_error_word(ws) == 0
+    assert_bitexact(bits(got), oracle.gemm_gelu_and_mul(bits(x.cpu()), bits(w.cpu())),
+                    "the call after the stall")

@@ -6,13 +6,21 @@ caller workspace.
 
 Called through the C ABI and checked against dtrot_gelu_and_mul (the entry
 point with a caller workspace) on two calls in a row, so the second call runs
-on the table the first one left in the shared array.  Runs alone in a fresh
-process as well as after the rest of the suite; the file name makes pytest
-collect it last.
+on the table the first one left in the shared array; the first call, which
+feeds every bf16 gate value, is also checked against the oracle.  A second
+test makes a noalloc call the very first library call of a fresh process (a
+child interpreter), where the array's address is looked up for the first
+time.  The file name makes pytest collect it last.
 """
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 from diffusion_transformer_elementwise_rotate_b300 import _capi
 from diffusion_transformer_elementwise_rotate_b300 import build as dbuild
@@ -64,6 +72,54 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(lib):
         got, exp = _geglu_both(lib, gu, F)
         assert_within_tolerance(got, exp, what)
         assert np.array_equal(got, exp), what   # the same kernels: identical bits
+        if what == "call 1":
+            ref = oracle.gelu_and_mul(gate, up)
+            assert_within_tolerance(got, ref, "call 1 against the oracle")
+
+
+_CHILD = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+from diffusion_transformer_elementwise_rotate_b300 import _capi
+from diffusion_transformer_elementwise_rotate_b300 import workloads as W
+T, F = 64, 1024
+gate = np.arange(1 << 16, dtype=np.uint16).reshape(T, F)
+up = W.normal_bf16((T, F), 23, 3).view(torch.int16).numpy().view(np.uint16)
+gu = torch.from_numpy(np.concatenate([gate, up], axis=1).view(np.int16)).view(
+    torch.bfloat16).cuda()
+outs = [torch.empty((T, F), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+st = torch.cuda.current_stream().cuda_stream
+lib = _capi.load()
+g, u = gu.data_ptr(), gu.data_ptr() + 2 * F
+# the first libdtrot call of this process: the array's address is looked up here
+rc = lib.dtrot_gelu_and_mul_noalloc(g, 2 * F, u, 2 * F, outs[0].data_ptr(), F, T, F, st)
+assert rc == _capi.OK, rc
+n = int(lib.dtrot_gelu_and_mul_workspace_bytes())
+ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+rc = lib.dtrot_gelu_and_mul(g, 2 * F, u, 2 * F, outs[1].data_ptr(), F, T, F, ws.data_ptr(), n,
+                            st)
+assert rc == _capi.OK, rc
+rc = lib.dtrot_gelu_and_mul_noalloc(g, 2 * F, u, 2 * F, outs[2].data_ptr(), F, T, F, st)
+assert rc == _capi.OK, rc
+torch.cuda.synchronize()
+bits = [o.cpu().view(torch.int16).numpy().view(np.uint16) for o in outs]
+np.save(sys.argv[2], np.stack(bits + [gate, up]))
+"""
+
+
+def test_noalloc_as_the_first_call_of_a_fresh_process(tmp_path):
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    dbuild.build()
+    dst = str(tmp_path / "out.npy")
+    r = subprocess.run([sys.executable, "-c", _CHILD, root, dst], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    first, ws_out, second, gate, up = np.load(dst)
+    assert np.array_equal(first, ws_out)
+    assert np.array_equal(second, ws_out)
+    assert_within_tolerance(first, oracle.gelu_and_mul(gate, up), "fresh process vs oracle")
 
 
 def test_noalloc_rejects_invalid_sizes_without_launching(lib):
