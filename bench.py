@@ -39,7 +39,8 @@ FALLBACK_HBM_GBS = 6400.0
 OPS = ["rope_cos_sin_precompute", "rope_rotate_half_q", "rope_rotate_half_k", "gelu_and_mul",
        "rmsnorm_residual_attn", "rmsnorm_residual_ffn"]
 DOMINANT = "gelu_and_mul"
-DOM_EVERY = 8  # timed steps per step whose dominant-kernel call is bracketed by events
+MIN_DOM_LAUNCHES = 20  # the dominant kernel's roofline is the median of at least this many calls
+PER_WORKLOAD = ("image", "cfg")  # other layer shapes reported beside the headline layer
 # kernels per step: tables 1, RoPE 2, GEGLU 2 (activation table + streaming), RMSNorm 2
 LAUNCHES_PER_STEP = 7
 
@@ -202,9 +203,9 @@ class ClockSampler:
 class Layer:
     """One layer's tensors on the device plus pinned host copies."""
 
-    def __init__(self, wl, W, dev):
+    def __init__(self, wl, W, dev, keep_host=True):
         self.wl = wl
-        pin = torch.cuda.is_available()
+        pin = torch.cuda.is_available() and keep_host
         self.h_in = {
             "freqs": W.freqs_for(wl).pin_memory() if pin else W.freqs_for(wl),
             "q": W.rope_inputs(wl, "q", pin=pin),
@@ -221,6 +222,9 @@ class Layer:
                        "q_out": e((B, S, H, D)), "k_out": e((B, S, H, D)),
                        "ff_out": e((wl.T_ff, F)), "y1": e((T, C)), "y2": e((T, C))})
         self.out_names = ["cos", "sin", "q_out", "k_out", "ff_out", "y1", "y2", "r1", "r2"]
+        if not keep_host:
+            self.h_in, self.h_out = {}, {}
+            return
         self.h_out = {n: torch.empty(self.d[n].shape, dtype=self.d[n].dtype, pin_memory=pin)
                       for n in self.out_names}
 
@@ -261,6 +265,63 @@ class Layer:
         for k in self.out_names:
             self.h_out[k].copy_(d[k], non_blocking=True)
         return sum(self.h_out[k].numel() * self.h_out[k].element_size() for k in self.out_names)
+
+
+def breakdown(dt, layer, steps):
+    """Per-op device time (ms, mean over `steps`) from a pass with CUDA events
+    between all kernels of the step."""
+    for _ in range(2):
+        layer.step(dt)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
+        layer.step(dt, evs[i])
+    torch.cuda.synchronize()
+    return {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+            for j, op in enumerate(OPS)}
+
+
+def other_workloads(dt, W, dev, steps, peak):
+    """The image and CFG layers: the same step on their shapes, timed like the
+    headline layer (a pass of plain steps, then a pass with events between the
+    kernels for the per-op figures), each on its own tensors.  Their steps move
+    0.71 and 1.42 GB, 5.6x and 11x the L2, so no op finds its inputs in L2 from
+    the step before (only the tables, which the step itself writes for RoPE)."""
+    res = {}
+    for name in PER_WORKLOAD:
+        wl = W.WORKLOADS[name]
+        layer = Layer(wl, W, dev, keep_host=False)
+        bts = step_bytes(wl, W)
+        per_step = sum(bts.values())
+        for _ in range(3):
+            layer.step(dt)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            layer.step(dt)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        km = breakdown(dt, layer, steps)
+        tokens = wl.B * wl.S
+        res[name] = {
+            "workload": config_for(wl, per_step, "replicas x1")["workload"],
+            "steps": steps,
+            "ms_per_step": round(ms, 5),
+            "gbs": round(per_step / (ms / 1e3) / 1e9, 1),
+            "frac_of_hbm_peak": round(per_step / (ms / 1e3) / 1e9 / peak, 4),
+            "mtokens_per_s_per_layer": round(
+                tokens / (sum(km[o] for o in OPS[1:]) / 1e3) / 1e6, 3),
+            "mtokens_per_s_per_step": round(tokens / (ms / 1e3) / 1e6, 3),
+            "kernels": {op: {"ms": round(km[op], 5), "bytes": bts[op],
+                             "gbs": round(bts[op] / (km[op] / 1e3) / 1e9, 1),
+                             "frac_of_hbm_peak": round(bts[op] / (km[op] / 1e3) / 1e9 / peak, 4)}
+                        for op in OPS},
+        }
+        del layer
+        torch.cuda.empty_cache()
+    return res
 
 
 def e2e_pipelined(dt, layer, steps):
@@ -372,7 +433,11 @@ def fused_mlp_geglu(dt, layer, wl, reps):
     """The MLP's gate_up projection with GEGLU in its epilogue (tcgen05), on the
     layer's pre-FFN norm output y2 (T, C) and random nn.Linear-style weights
     (2F, C) ~ U(-1/sqrt C, 1/sqrt C); next to cuBLAS (torch.matmul) writing
-    gate_up followed by gelu_and_mul.  TFLOP/s count 2 * T * C * 2F."""
+    gate_up followed by gelu_and_mul.  TFLOP/s count 2 * T * C * 2F.  The three
+    calls are timed interleaved (fused, matmul, gelu_and_mul, fused, ...), each
+    between its own CUDA events, so that all of them see the same clock and
+    power state (at the 1.1 kW limit the SM clock of a long GEMM run drifts by
+    10-20%); the figures are medians over `reps` rounds."""
     d = layer.d
     x = d["y2"]
     T, C = x.shape
@@ -383,36 +448,39 @@ def fused_mlp_geglu(dt, layer, wl, reps):
     out = torch.empty((T, F), dtype=torch.bfloat16, device=x.device)
     gu = torch.empty((T, 2 * F), dtype=torch.bfloat16, device=x.device)
     flops = 2.0 * T * C * 2 * F
-
-    def timed(fn):
-        for _ in range(2):
+    calls = {"fused": lambda: dt.gemm_gelu_and_mul(x, w, out=out),
+             "matmul": lambda: torch.matmul(x, w.t(), out=gu),
+             "act": lambda: dt.gelu_and_mul(gu[:, :F], gu[:, F:], out=out)}
+    for _ in range(2):
+        for fn in calls.values():
             fn()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(reps):
+    torch.cuda.synchronize()
+    evs = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)] for k in calls}
+    for i in range(reps):
+        for k, fn in calls.items():
+            evs[k][i][0].record()
             fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
-
-    ms_fused = timed(lambda: dt.gemm_gelu_and_mul(x, w, out=out))
-    ms_mm = timed(lambda: torch.matmul(x, w.t(), out=gu))
-    ms_act = timed(lambda: dt.gelu_and_mul(gu[:, :F], gu[:, F:], out=out))
+            evs[k][i][1].record()
+    torch.cuda.synchronize()
+    med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in evs.items()}
+    ms_fused, ms_mm, ms_act = med["fused"], med["matmul"], med["act"]
     del w, out, gu
     peak, kind = tensor_peak()
     tf = flops / ms_fused / 1e9
     return {"gemm_gelu_and_mul": {"ms": round(ms_fused, 4), "tflops": round(tf, 1),
                                   "launches": 2, "reps": reps,
                                   "shape": f"x ({T}, {C}) x w ({2 * F}, {C})^T -> ({T}, {F})",
+                                  "how": "median of per-call CUDA-event times, interleaved with "
+                                         "the cuBLAS matmul and gelu_and_mul calls",
                                   "roofline": {"bound": "tensor", "achieved": round(tf, 1),
                                                "peak": peak, "unit": "TFLOP/s",
                                                "frac": round(tf / peak, 4),
                                                "peak_kind": kind}},
             "cublas_matmul_then_gelu_and_mul": {
                 "ms": round(ms_mm + ms_act, 4), "matmul_ms": round(ms_mm, 4),
-                "matmul_tflops": round(flops / ms_mm / 1e9, 1), "gelu_and_mul_ms": round(ms_act, 4)}}
+                "matmul_tflops": round(flops / ms_mm / 1e9, 1), "gelu_and_mul_ms": round(ms_act, 4),
+                "fused_over_matmul": round(ms_fused / ms_mm, 4)}}
 
 
 def cpu_baseline(wl, W, layer, target_s=15.0):
@@ -501,47 +569,49 @@ def native(args):
     bts = step_bytes(wl, W)
     per_step = sum(bts.values())
 
-    for _ in range(max(3, args.warmup)):
-        layer.step(dt)
-    torch.cuda.synchronize()
-
     K = args.steps
-    # the timed steps record events only around the dominant kernel (its
-    # roofline), in every DOM_EVERY-th step; events between all kernels would
-    # add ~16 us per step and stop the launches from overlapping (each launch is
-    # a programmatic dependent of the one before), so the per-op breakdown is a
-    # separate pass below
-    jd = OPS.index(DOMINANT)
-    sampled = [i for i in range(K) if i % DOM_EVERY == 0]
-    dom_evs = [[torch.cuda.Event(enable_timing=True) if (j in (jd, jd + 1) and i % DOM_EVERY == 0)
-                else None for j in range(7)] for i in range(K)]
+    warm = max(3, args.warmup)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
+    # warm-up steps directly before the timed region (no idle gap in between)
+    for _ in range(warm):
+        layer.step(dt)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
+    # the timed steps record no events between kernels: an event between two
+    # launches costs ~2 us and stops the second from starting as the
+    # programmatic dependent of the first
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
     for i in range(K):
-        layer.step(dt, dom_evs[i])
+        layer.step(dt)
     t_end.record()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    clocks = sampler.stop() if rank == 0 else None
     elapsed_ms = t_start.elapsed_time(t_end)
-    dom_ms = sum(dom_evs[i][jd].elapsed_time(dom_evs[i][jd + 1]) for i in sampled) / len(sampled)
-    # per-op breakdown: a separate pass with events between all kernels
-    KB = min(K, 100)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(KB)]
-    for i in range(KB):
-        layer.step(dt, evs[i])
+    # the dominant kernel: a second pass with events around its call (both of
+    # its launches, the activation table and the streaming kernel) in every
+    # step, at least MIN_DOM_LAUNCHES calls; median, min and max per call
+    jd = OPS.index(DOMINANT)
+    KD = max(K, MIN_DOM_LAUNCHES)
+    dom_evs = [[torch.cuda.Event(enable_timing=True) if j in (jd, jd + 1) else None
+                for j in range(7)] for _ in range(KD)]
+    for _ in range(2):
+        layer.step(dt)
+    for i in range(KD):
+        layer.step(dt, dom_evs[i])
     torch.cuda.synchronize()
-    kern_ms = {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(KB)) / KB
-               for j, op in enumerate(OPS)}
+    clocks = sampler.stop() if rank == 0 else None
+    dom_all = sorted(dom_evs[i][jd].elapsed_time(dom_evs[i][jd + 1]) for i in range(KD))
+    dom_ms = statistics.median(dom_all)
+    # per-op breakdown: a separate pass with events between all kernels
+    KB = min(max(K, 20), 100)
+    kern_ms = breakdown(dt, layer, KB)
     elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
     ms_per_step = elapsed_ms / K
     value = aggregate_gbs(per_step, world, K, elapsed_ms)
@@ -549,8 +619,13 @@ def native(args):
     # beyond the step, on the same layer: RoPE on q and k in one in-place launch,
     # with the tables or with the angles evaluated inside the kernel
     fused = fused_rope_qk(dt, layer, wl, min(K, 200))
-    fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))
     fused.update(geglu_prebuilt_table(dt, layer, wl, min(K, 200)))
+
+    peak, peak_kind = peaks()
+    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak)
+    # the GEMM last: at the 1.1 kW power limit it leaves the GPU slower for a
+    # while (memory-bound kernels timed right after it read 15-20% low)
+    fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))
 
     # end to end through host buffers: H2D inputs, the step, D2H outputs,
     # pipelined across steps on three streams
@@ -569,7 +644,6 @@ def native(args):
         if pg:
             pg.destroy_process_group()
         return
-    peak, peak_kind = peaks()
     achieved = bts[DOMINANT] / (dom_ms / 1e3) / 1e9
     tokens = wl.B * wl.S
     line = {
@@ -598,14 +672,21 @@ def native(args):
                        + kern_ms["rmsnorm_residual_attn"] + kern_ms["rmsnorm_residual_ffn"])
                       / 1e3) / 1e6, 3),
         "kernels": {op: {"ms": round(kern_ms[op], 5), "bytes": bts[op],
-                         "gbs": round(bts[op] / (kern_ms[op] / 1e3) / 1e9, 1)} for op in OPS},
+                         "gbs": round(bts[op] / (kern_ms[op] / 1e3) / 1e9, 1),
+                         "frac_of_hbm_peak": round(bts[op] / (kern_ms[op] / 1e3) / 1e9 / peak, 4)}
+                    for op in OPS},
         "kernels_how": (f"a separate pass of {KB} steps with CUDA events between all kernels; "
                         "the events cost time and stop consecutive launches from overlapping, "
                         "so these times add up to more than ms_per_step"),
         "roofline": {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
-                     "ms": round(dom_ms, 5), "launches_timed": len(sampled),
-                     "how": f"CUDA events around the kernel's call in every {DOM_EVERY}th timed "
-                            "step",
+                     "ms": round(dom_ms, 5), "ms_min": round(dom_all[0], 5),
+                     "ms_max": round(dom_all[-1], 5), "launches_timed": KD,
+                     "how": (f"median over {KD} calls of the time between CUDA events around the "
+                             "kernel's call, in every step of a pass of the same layer steps "
+                             "after the timed ones; the bracket holds both of the call's "
+                             "launches (the 7 us activation-table kernel and the streaming "
+                             "kernel); the events also keep the call from overlapping its "
+                             "neighbours, which the unbracketed timed steps allow"),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
                      "algorithmic_bytes": bts[DOMINANT]},
@@ -616,6 +697,7 @@ def native(args):
                        "three streams with two device sets"},
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "next_rows": fused,
+        "per_workload": per_wl,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
