@@ -94,17 +94,26 @@ __device__ __forceinline__ uint16_t rn16d(double d) {
 // idle almost always.
 constexpr int kCosSinMargin = 4;
 
+// The fp64 recomputations, out of line: they run for a few entries in 10^4,
+// and inlined at every call site they made the table kernel's code large
+// enough to stall on instruction fetch.
+static __device__ __noinline__ float cos_exact_f32(float f) { return __double2float_rn(cos((double)f)); }
+static __device__ __noinline__ float sin_exact_f32(float f) { return __double2float_rn(sin((double)f)); }
+
 __device__ __forceinline__ void cos_sin_entry(float f, uint16_t& c16, uint16_t& s16) {
     float s32, c32;
     sincosf(f, &s32, &c32);
-    if (ulps_to_bf16_midpoint(c32) <= kCosSinMargin) {
-        c32 = __double2float_rn(cos((double)f));
-    }
-    if (ulps_to_bf16_midpoint(s32) <= kCosSinMargin) {
-        s32 = __double2float_rn(sin((double)f));
-    }
+    if (ulps_to_bf16_midpoint(c32) <= kCosSinMargin) c32 = cos_exact_f32(f);
+    if (ulps_to_bf16_midpoint(s32) <= kCosSinMargin) s32 = sin_exact_f32(f);
     c16 = rn16f(c32);
     s16 = rn16f(s32);
+}
+
+// The same entry through a call (for paths that rarely need it).
+static __device__ __noinline__ uint32_t cos_sin_entry_call(float f) {
+    uint16_t c, s;
+    cos_sin_entry(f, c, s);
+    return (uint32_t)c | ((uint32_t)s << 16);
 }
 
 // ------------------------------------------------------------ GELU table entries
@@ -190,17 +199,15 @@ struct RmsParams {
 // ------------------------------------------------------------ launch order
 //
 // The library's kernels are launched as programmatic dependents of the
-// previous kernel in the stream: a launch may be scheduled while its
-// predecessor finishes, which hides the launch and ramp-up between the short
-// memory-bound kernels of a step.  Every kernel therefore executes pdl_wait()
-// before its first global-memory access, read or write; pdl_wait returns once
-// the predecessor has completed and its writes are visible (at once when the
-// launch has no programmatic predecessor), so every memory effect keeps plain
-// stream order.  pdl_launch_dependents() lets the next launch be scheduled
-// before this one ends; it never lets the next kernel past its own pdl_wait().
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+// previous kernel in the stream.  None of the elementwise kernels triggers its
+// dependents early: the next launch is scheduled as this kernel's CTAs exit,
+// which overlaps its launch latency and ramp-up with this kernel's drain, and
+// its CTAs never sit on an SM beside running CTAs of this kernel (an early
+// trigger was measured equal on the video layer and 1-1.5% slower on the image
+// and CFG layers).  Every kernel executes pdl_wait() before its first
+// global-memory access, read or write; pdl_wait returns once the predecessor
+// has completed and its writes are visible (at once when the launch has no
+// programmatic predecessor), so every memory effect keeps plain stream order.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>

@@ -46,17 +46,19 @@ __device__ __forceinline__ uint4 geglu_vec(const uint16_t* tab, uint4 g, uint4 u
 }
 
 
-// One table entry per thread: table[i] = RN16(RN32(gelu(bf16 bits i))).
+// One table entry per thread: table[i] = RN16(RN32(gelu(bf16 bits i))).  The
+// entry depends on nothing in memory, so it is computed while the previous
+// kernel in the stream may still be running; only the store waits for it (it
+// may still read this workspace).
 __global__ void __launch_bounds__(256) gelu_table_kernel(uint16_t* __restrict__ table) {
-    pdl_launch_dependents();
-    pdl_wait();  // the previous kernel may still read this workspace
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < kTable) table[i] = gelu_entry((uint32_t)i);
+    const uint16_t v = i < kTable ? gelu_entry((uint32_t)i) : (uint16_t)0;
+    pdl_wait();
+    if (i < kTable) table[i] = v;
 }
 
 // Copies the table from the workspace into shared memory (16 bytes per load).
 __device__ __forceinline__ void load_table(uint16_t* tab, const uint16_t* __restrict__ gtab) {
-    pdl_launch_dependents();
     pdl_wait();  // the table kernel (or whatever ran before) has completed
     const uint4* src = reinterpret_cast<const uint4*>(gtab);
     uint4* dst = reinterpret_cast<uint4*>(tab);

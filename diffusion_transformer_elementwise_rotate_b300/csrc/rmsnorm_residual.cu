@@ -355,7 +355,6 @@ __device__ __forceinline__ void load_w(const RmsParams& p, int nv, uint4 (&wv)[V
 template <int VPT>
 __global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
     __shared__ RowShared sh;
-    pdl_launch_dependents();
     pdl_wait();
     const int nv = (int)(p.C >> 3);
     const int tid = threadIdx.x;
@@ -393,7 +392,6 @@ __global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
 // accumulates; pass 2 re-reads the thread's own h values.
 __global__ void __launch_bounds__(256) rms_generic_kernel(RmsParams p) {
     __shared__ RowShared sh;
-    pdl_launch_dependents();
     pdl_wait();
     int slot = 0;
     for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, slot ^= 1) {

@@ -18,15 +18,40 @@
 namespace dtrot {
 namespace {
 
+__device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
+    return make_uint4(v[0] | ((uint32_t)v[1] << 16), v[2] | ((uint32_t)v[3] << 16),
+                      v[4] | ((uint32_t)v[5] << 16), v[6] | ((uint32_t)v[7] << 16));
+}
+
+// Eight consecutive angles -> their cos and sin entries.
+__device__ __forceinline__ void entries8(const float (&f)[8], uint16_t (&c)[8],
+                                         uint16_t (&sn)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cos_sin_entry(f[k], c[k], sn[k]);
+}
+
+__device__ __forceinline__ void load8(const float* src, float (&f)[8]) {
+    const float4 f0 = __ldg(reinterpret_cast<const float4*>(src));
+    const float4 f1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
+    f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
+    f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
+}
+
 // VEC = 8: R % 8 == 0 and every base pointer 16-byte aligned (freqs 32-byte).
-template <int VEC>
+// PAIR (R % 16 == 0): a thread takes columns j..j+7 of the first half of the
+// row and the same columns of the second half, j+R/2..; a second-half angle
+// whose bits equal its first-half partner's has the same entry, which is then
+// copied instead of evaluated again (a rotate-half table built from per-axis
+// angles repeats its half-row, so this halves the arithmetic there; any other
+// angle is evaluated, so nothing is assumed about the layout).
+template <int VEC, bool PAIR>
 __global__ void __launch_bounds__(256) rope_cos_sin_kernel(const float* __restrict__ freqs,
                                                           int64_t S, int64_t B, int64_t R,
                                                           uint16_t* __restrict__ cos_out,
                                                           uint16_t* __restrict__ sin_out) {
-    pdl_launch_dependents();
     pdl_wait();
-    const int64_t groups_per_row = R / VEC;
+    const int64_t span = PAIR ? R / 2 : R;  // columns whose groups a thread starts at
+    const int64_t groups_per_row = span / VEC;
     const int64_t total = B * S * groups_per_row;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
          g += (int64_t)gridDim.x * blockDim.x) {
@@ -37,23 +62,27 @@ __global__ void __launch_bounds__(256) rope_cos_sin_kernel(const float* __restri
         const float* src = freqs + (s * B + b) * R + j;
         const int64_t dst = row * R + j;
         if constexpr (VEC == 8) {
-            float4 f0 = __ldg(reinterpret_cast<const float4*>(src));
-            float4 f1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
-            float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+            float f[8];
             uint16_t c[8], sn[8];
+            load8(src, f);
+            entries8(f, c, sn);
+            *reinterpret_cast<uint4*>(cos_out + dst) = pack8(c);
+            *reinterpret_cast<uint4*>(sin_out + dst) = pack8(sn);
+            if constexpr (PAIR) {
+                const int64_t h = R / 2;
+                float f2[8];
+                load8(src + h, f2);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) cos_sin_entry(f[k], c[k], sn[k]);
-            uint4 cv, sv;
-            cv.x = c[0] | ((uint32_t)c[1] << 16);
-            cv.y = c[2] | ((uint32_t)c[3] << 16);
-            cv.z = c[4] | ((uint32_t)c[5] << 16);
-            cv.w = c[6] | ((uint32_t)c[7] << 16);
-            sv.x = sn[0] | ((uint32_t)sn[1] << 16);
-            sv.y = sn[2] | ((uint32_t)sn[3] << 16);
-            sv.z = sn[4] | ((uint32_t)sn[5] << 16);
-            sv.w = sn[6] | ((uint32_t)sn[7] << 16);
-            *reinterpret_cast<uint4*>(cos_out + dst) = cv;
-            *reinterpret_cast<uint4*>(sin_out + dst) = sv;
+                for (int k = 0; k < 8; ++k) {
+                    if (__float_as_uint(f2[k]) != __float_as_uint(f[k])) {
+                        const uint32_t e = cos_sin_entry_call(f2[k]);
+                        c[k] = (uint16_t)e;
+                        sn[k] = (uint16_t)(e >> 16);
+                    }
+                }
+                *reinterpret_cast<uint4*>(cos_out + dst + h) = pack8(c);
+                *reinterpret_cast<uint4*>(sin_out + dst + h) = pack8(sn);
+            }
         } else {
             uint16_t c, sn;
             cos_sin_entry(__ldg(src), c, sn);
@@ -71,16 +100,20 @@ cudaError_t launch_rope_cos_sin(const float* freqs, int64_t S, int64_t B, int64_
                                 uint16_t* cos_out, uint16_t* sin_out, cudaStream_t st) {
     const bool vec = (R % 8 == 0) && aligned(freqs, 32) && aligned(cos_out, 16) &&
                      aligned(sin_out, 16);
-    const int64_t work = B * S * (vec ? R / 8 : R);
+    const bool pair = vec && (R % 16 == 0);
+    const int64_t work = B * S * (pair ? R / 16 : vec ? R / 8 : R);
     const int threads = 256;
     int64_t blocks = (work + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident blocks of 256 per SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    return vec ? launch_pdl(rope_cos_sin_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, st,
-                            freqs, S, B, R, cos_out, sin_out)
-               : launch_pdl(rope_cos_sin_kernel<1>, dim3((unsigned)blocks), dim3(threads), 0, st,
-                            freqs, S, B, R, cos_out, sin_out);
+    if (pair)
+        return launch_pdl(rope_cos_sin_kernel<8, true>, dim3((unsigned)blocks), dim3(threads), 0,
+                          st, freqs, S, B, R, cos_out, sin_out);
+    return vec ? launch_pdl(rope_cos_sin_kernel<8, false>, dim3((unsigned)blocks), dim3(threads),
+                            0, st, freqs, S, B, R, cos_out, sin_out)
+               : launch_pdl(rope_cos_sin_kernel<1, false>, dim3((unsigned)blocks), dim3(threads),
+                            0, st, freqs, S, B, R, cos_out, sin_out);
 }
 
 }  // namespace dtrot

@@ -85,7 +85,6 @@ template <int VW, int U, bool ANGLES>
 __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
     using V = typename QKVec<VW>::T;
     __shared__ __align__(16) uint16_t cs[kWarps][2][kMaxRot];  // angle mode: cos, sin row
-    pdl_launch_dependents();
     pdl_wait();
     const RopeQKParams& p = a.p;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -172,7 +171,6 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
 // [0, Hq) are q's, [Hq, Hq + Hk) k's.
 template <bool ANGLES>
 __global__ void __launch_bounds__(256) rope_qk_generic_kernel(RopeQKParams p) {
-    pdl_launch_dependents();
     pdl_wait();
     const int64_t hh = p.rot >> 1;
     const int64_t rows = p.Hq + p.Hk;

@@ -80,7 +80,6 @@ struct FastArgs {
 
 template <int VW, int U>
 __global__ void __launch_bounds__(256) rope_fast_kernel(FastArgs a) {
-    pdl_launch_dependents();
     pdl_wait();
     using V = typename VecT<VW>::T;
     const RopeParams& p = a.p;
@@ -147,7 +146,6 @@ __global__ void __launch_bounds__(256) rope_fast_kernel(FastArgs a) {
 // Generic path: one thread per (token, head, item); item < h is the pair
 // (j, j + h), item >= h is tail column rot + (item - h).
 __global__ void __launch_bounds__(256) rope_generic_kernel(RopeParams p, int64_t items) {
-    pdl_launch_dependents();
     pdl_wait();
     const int64_t hh = p.rot >> 1;
     const int64_t per_tok = p.H * items;

@@ -76,6 +76,28 @@ def test_cos_sin_many_angles_near_rounding_midpoints():
     assert_bitexact(bits(s), es, "sin")
 
 
+def test_cos_sin_second_half_reused_only_for_identical_bits():
+    # rows of 32 angles (R % 16 == 0: the kernel pairs column j with j + 16 and
+    # copies j's entry when the two angles have the same bits): equal halves,
+    # halves that differ in one column, +0 against -0 (equal values, different
+    # sin), NaNs with different payloads, and random halves
+    g = torch.Generator().manual_seed(29)
+    S, B, R = 515, 2, 32
+    f = (torch.rand((S, B, 1, R), generator=g) * 400.0 - 200.0)
+    f[: S // 2, :, :, R // 2:] = f[: S // 2, :, :, : R // 2]
+    f[1::7, :, :, R // 2 + 3] += 1.0
+    f[2, 0, 0, 5], f[2, 0, 0, R // 2 + 5] = 0.0, -0.0
+    f[3, 1, 0, 6], f[3, 1, 0, R // 2 + 6] = -0.0, 0.0
+    nan_a = np.array([0x7FC00001], dtype=np.uint32).view(np.float32)[0]
+    nan_b = np.array([0xFFC00002], dtype=np.uint32).view(np.float32)[0]
+    f[4, 0, 0, 1], f[4, 0, 0, R // 2 + 1] = float(nan_a), float(nan_b)
+    f = f.contiguous()
+    c, s = dt.rope_cos_sin_precompute(to_dev(f))
+    ec, es = oracle.rope_cos_sin(f.numpy())
+    assert_bitexact(bits(c), ec, "cos")
+    assert_bitexact(bits(s), es, "sin")
+
+
 def test_cos_sin_reduction_range_and_zero_crossings():
     # Angles where the table kernel's hardware sine/cosine path ends: uniform over
     # [-4100, 4100] (that path reduces |f| <= 4096 by 2 pi), next to every multiple
@@ -665,3 +687,45 @@ def test_back_to_back_calls_keep_stream_order():
         h, y = oracle.rmsnorm_residual(bits(x), h, bits(w), EPS)
         assert_within_tolerance(bits(ys[i]), y, f"rmsnorm {i}")
     assert_bitexact(bits(rd), h, "residual after three calls")
+
+
+# ---------------------------------------------------------------- 2^14 elements per op
+
+# The smallest sizes of the shape sweep: grids larger than the work (persistent
+# RMSNorm and GEGLU grids with more CTAs than rows, RoPE with fewer token warps
+# than SMs), element by element against the oracle.
+SMALL = 1 << 14
+
+
+@pytest.mark.parametrize("C", [768, 2560, 4096, 5120])
+def test_rmsnorm_2_14_elements(C):
+    T = max(1, SMALL // C)
+    x = W.normal_bf16((T, C), 300 + C, 4)
+    r = W.normal_bf16((T, C), 300 + C, 5, std=2.0)
+    w = W.normal_bf16((C,), 300 + C, 6, mean=1.0, std=0.316)
+    _rms_check(x, r, w, None, f"T={T} C={C}")
+
+
+@pytest.mark.parametrize("F", [768, 2560, 4096, 5120])
+def test_geglu_2_14_elements(F):
+    T = max(1, SMALL // F)
+    gu = W.normal_bf16((T, 2 * F), 310 + F, 2)
+    _geglu_check(gu, F, None, f"T={T} F={F}")
+
+
+@pytest.mark.parametrize("S", [16, 5])
+@pytest.mark.parametrize("D,rot", SWEEP)
+def test_rope_2_14_elements(D, rot, S):
+    B = 1
+    H = max(1, SMALL // (S * D))
+    x = W.normal_bf16((B, S, H, D), 320 + D + rot + S, 0)
+    freqs = W.freqs_1d(S, B, rot)
+    cos_b, sin_b = oracle.rope_cos_sin(freqs.numpy())
+    got_c, got_s = dt.rope_cos_sin_precompute(to_dev(freqs))
+    torch.cuda.synchronize()
+    assert_bitexact(bits(got_c), cos_b, "cos")
+    assert_bitexact(bits(got_s), sin_b, "sin")
+    exp = oracle.rope_rotate_half(bits(x), cos_b, sin_b)
+    assert_bitexact(_rope_case(x, cos_b, sin_b), exp, f"S={S} H={H} D={D} rot={rot}")
+    for mode in ("tables", "angles"):
+        _qk_check(B, S, H, max(1, H // 4), D, rot, freqs, 330 + D + rot + S, mode)
