@@ -126,24 +126,30 @@ def step_bytes(wl, W):
     }
 
 
-def source_hash(name: str) -> str:
-    with open(os.path.join(ROOT, PKG, "csrc", name), "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+def source_hash(*names: str) -> str:
+    """sha256 prefix of the named csrc files, concatenated in order."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, PKG, "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
-def recorded_traffic(wl_name: str):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu
-    summary, if it was taken on the current source of that kernel."""
-    path = os.path.join(ROOT, "profiles", "gelu_and_mul_traffic.json")
+def recorded_traffic(wl_name: str, op: str = DOMINANT):
+    """DRAM bytes per launch of an op's kernel on the video layer, from the
+    committed ncu record, if it was taken on the current source of that kernel
+    (its .cu file and the shared header); else None."""
+    if wl_name != "video":
+        return None
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as fh:
-            d = json.load(fh)
+            k = json.load(fh)["kernels"][op]
     except Exception:
         return None
-    if d.get("source_sha256_16") != source_hash("gelu_and_mul.cu"):
+    if k.get("source_sha256_16") != source_hash(k["source"], "dtrot_internal.cuh"):
         return None
-    per = d.get("per_workload", {}).get(wl_name)
-    return None if per is None else float(per["dram_bytes_per_launch"])
+    return float(k["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -267,17 +273,63 @@ class Layer:
         return sum(self.h_out[k].numel() * self.h_out[k].element_size() for k in self.out_names)
 
 
+def step_graph(dt, layer, steps, evs=None):
+    """A CUDA graph of `steps` layer steps (evs[i]: the 7 events of step i, or
+    None).  The steps' kernels keep their programmatic-dependent edges inside
+    the graph, and replaying it costs one host call, so the timed passes measure
+    the GPU alone, not the Python launch path (on a busy host that path could
+    fall behind the short kernels).  Events given are external: they become
+    event-record nodes whose times elapsed_time() reads after a replay."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            layer.step(dt)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(steps):
+            layer.step(dt, None if evs is None else evs[i])
+    torch.cuda.synchronize()
+    return g
+
+
+def timing_events(n, which=range(7)):
+    """n sets of 7 external timing events (None where not in `which`)."""
+    return [[torch.cuda.Event(enable_timing=True, external=True) if j in which else None
+             for j in range(7)] for _ in range(n)]
+
+
 def breakdown(dt, layer, steps):
     """Per-op device time (ms, mean over `steps`) from a pass with CUDA events
-    between all kernels of the step."""
-    for _ in range(2):
-        layer.step(dt)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
-    for i in range(steps):
-        layer.step(dt, evs[i])
+    between all kernels of the step (a graph of `steps` steps, replayed once)."""
+    evs = timing_events(steps)
+    g = step_graph(dt, layer, steps, evs)
+    g.replay()
     torch.cuda.synchronize()
-    return {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
-            for j, op in enumerate(OPS)}
+    res = {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+           for j, op in enumerate(OPS)}
+    del g
+    return res
+
+
+def timed_steps(dt, layer, steps, warm):
+    """ms for `steps` layer steps: one replay of a graph of `steps` steps
+    between two events, after `warm` replays of a one-step graph."""
+    g1 = step_graph(dt, layer, 1)
+    gk = step_graph(dt, layer, steps)
+    for _ in range(warm):
+        g1.replay()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    gk.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    del g1, gk
+    return ms
 
 
 def other_workloads(dt, W, dev, steps, peak):
@@ -292,17 +344,7 @@ def other_workloads(dt, W, dev, steps, peak):
         layer = Layer(wl, W, dev, keep_host=False)
         bts = step_bytes(wl, W)
         per_step = sum(bts.values())
-        for _ in range(3):
-            layer.step(dt)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            layer.step(dt)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
+        ms = timed_steps(dt, layer, steps, 3) / steps
         km = breakdown(dt, layer, steps)
         tokens = wl.B * wl.S
         res[name] = {
@@ -571,45 +613,46 @@ def native(args):
 
     K = args.steps
     warm = max(3, args.warmup)
+    # the passes run as CUDA graphs (captured before the clock sampler starts):
+    # the K timed steps as one graph with no events between kernels (an event
+    # between two launches costs ~2 us and stops the second from starting as
+    # the programmatic dependent of the first); the dominant kernel with events
+    # around its call (both of its launches, the activation table and the
+    # streaming kernel) in every step of a second graph of at least
+    # MIN_DOM_LAUNCHES steps (median, min and max per call)
+    g1 = step_graph(dt, layer, 1)
+    gk = step_graph(dt, layer, K)
+    jd = OPS.index(DOMINANT)
+    KD = max(K, MIN_DOM_LAUNCHES)
+    dom_evs = timing_events(KD, (jd, jd + 1))
+    gd = step_graph(dt, layer, KD, dom_evs)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
     # warm-up steps directly before the timed region (no idle gap in between)
     for _ in range(warm):
-        layer.step(dt)
+        g1.replay()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    # the timed steps record no events between kernels: an event between two
-    # launches costs ~2 us and stops the second from starting as the
-    # programmatic dependent of the first
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for i in range(K):
-        layer.step(dt)
+    gk.replay()
     t_end.record()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    # the dominant kernel: a second pass with events around its call (both of
-    # its launches, the activation table and the streaming kernel) in every
-    # step, at least MIN_DOM_LAUNCHES calls; median, min and max per call
-    jd = OPS.index(DOMINANT)
-    KD = max(K, MIN_DOM_LAUNCHES)
-    dom_evs = [[torch.cuda.Event(enable_timing=True) if j in (jd, jd + 1) else None
-                for j in range(7)] for _ in range(KD)]
-    for _ in range(2):
-        layer.step(dt)
-    for i in range(KD):
-        layer.step(dt, dom_evs[i])
+    g1.replay()
+    gd.replay()
     torch.cuda.synchronize()
     clocks = sampler.stop() if rank == 0 else None
     dom_all = sorted(dom_evs[i][jd].elapsed_time(dom_evs[i][jd + 1]) for i in range(KD))
     dom_ms = statistics.median(dom_all)
-    # per-op breakdown: a separate pass with events between all kernels
+    del g1, gk, gd
+    # per-op breakdown: a separate graph with events between all kernels
     KB = min(max(K, 20), 100)
     kern_ms = breakdown(dt, layer, KB)
     elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
@@ -675,15 +718,15 @@ def native(args):
                          "gbs": round(bts[op] / (kern_ms[op] / 1e3) / 1e9, 1),
                          "frac_of_hbm_peak": round(bts[op] / (kern_ms[op] / 1e3) / 1e9 / peak, 4)}
                     for op in OPS},
-        "kernels_how": (f"a separate pass of {KB} steps with CUDA events between all kernels; "
+        "kernels_how": (f"a separate graph of {KB} steps with CUDA events between all kernels; "
                         "the events cost time and stop consecutive launches from overlapping, "
                         "so these times add up to more than ms_per_step"),
         "roofline": {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
                      "ms": round(dom_ms, 5), "ms_min": round(dom_all[0], 5),
                      "ms_max": round(dom_all[-1], 5), "launches_timed": KD,
                      "how": (f"median over {KD} calls of the time between CUDA events around the "
-                             "kernel's call, in every step of a pass of the same layer steps "
-                             "after the timed ones; the bracket holds both of the call's "
+                             "kernel's call, in every step of a graph of the same layer steps "
+                             "replayed after the timed ones; the bracket holds both of the call's "
                              "launches (the 7 us activation-table kernel and the streaming "
                              "kernel); the events also keep the call from overlapping its "
                              "neighbours, which the unbracketed timed steps allow"),
@@ -695,6 +738,9 @@ def native(args):
                 "how": "every step uploads all inputs from pinned host memory and downloads all "
                        "outputs; uploads, compute and downloads of consecutive steps overlap on "
                        "three streams with two device sets"},
+        "launch": ("the K timed steps run as one CUDA graph (captured before timing; the "
+                   "kernels' programmatic-dependent edges are kept inside it), replayed once "
+                   "between two CUDA events"),
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "next_rows": fused,
         "per_workload": per_wl,

@@ -20,8 +20,10 @@ a capture can hold a slice of a layer that still exceeds the 126 MB L2.
 Inputs are drawn on the device (torch's CUDA generator, seed 0) with the
 workload's distributions: timing does not depend on the values, and drawing a
 few GB on the host would dominate a short run.  Every launch is bracketed by
-CUDA events on the current stream; the line reports the median, min and max
-per launch, the algorithmic bytes (or flops) and the rate.
+CUDA events; the line reports the median, min and max per launch, the mean of
+the same number of launches back to back, the algorithmic bytes (or flops)
+and the rates.  By default the launches run as CUDA graphs (--eager: one
+Python call at a time).
 """
 from __future__ import annotations
 
@@ -107,27 +109,68 @@ def setup(op: str, wl: W.Workload, rows: int | None, dev):
     raise ValueError(f"unknown op {op!r}; one of {OPS}")
 
 
+def _graph(fn, n, evs=None):
+    """A CUDA graph of n calls of fn (evs[i]: external events around call i)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            if evs is not None:
+                evs[i][0].record()
+            fn()
+            if evs is not None:
+                evs[i][1].record()
+    torch.cuda.synchronize()
+    return g
+
+
 def run(op: str, workload: str = "video", rows: int | None = None, reps: int = 20,
-        warmup: int = 3) -> dict:
+        warmup: int = 3, graph: bool = True) -> dict:
+    """Per-launch times (events around each call) and the back-to-back rate
+    (reps calls between two events).  With graph=True both run as CUDA graphs,
+    so that host launch overhead never shows in the times (a short kernel
+    launched from Python one call at a time can leave the GPU waiting)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     fn, work, unit, desc, _live = setup(op, W.WORKLOADS[workload], rows, dev)
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
-    for e0, e1 in evs:
-        e0.record()
-        fn()
-        e1.record()
+    evs = [(torch.cuda.Event(enable_timing=True, external=graph),
+            torch.cuda.Event(enable_timing=True, external=graph)) for _ in range(reps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if graph:
+        g_each, g_b2b = _graph(fn, reps, evs), _graph(fn, reps)
+        g_each.replay()
+        t0.record()
+        g_b2b.replay()
+        t1.record()
+    else:
+        for e0, e1 in evs:
+            e0.record()
+            fn()
+            e1.record()
+        t0.record()
+        for _ in range(reps):
+            fn()
+        t1.record()
     torch.cuda.synchronize()
     ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     med = statistics.median(ms)
-    rate = work / (med / 1e3) / (1e9 if unit == "B" else 1e12)
+    b2b = t0.elapsed_time(t1) / reps
+    scale = 1e9 if unit == "B" else 1e12
     return {"op": op, "case": desc, "launch_ms_median": round(med, 5),
             "launch_ms_min": round(min(ms), 5), "launch_ms_max": round(max(ms), 5),
-            "reps": reps, "work": work, "work_unit": unit,
-            "rate": round(rate, 1), "rate_unit": "GB/s" if unit == "B" else "TFLOP/s"}
+            "back_to_back_ms": round(b2b, 5), "reps": reps, "graph": graph,
+            "work": work, "work_unit": unit,
+            "rate": round(work / (med / 1e3) / scale, 1),
+            "rate_back_to_back": round(work / (b2b / 1e3) / scale, 1),
+            "rate_unit": "GB/s" if unit == "B" else "TFLOP/s"}
 
 
 def main():
@@ -137,8 +180,10 @@ def main():
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--eager", action="store_true",
+                    help="launch from Python one call at a time instead of CUDA graphs")
     a = ap.parse_args()
-    print(json.dumps(run(a.op, a.workload, a.rows, a.reps, a.warmup)), flush=True)
+    print(json.dumps(run(a.op, a.workload, a.rows, a.reps, a.warmup, not a.eager)), flush=True)
 
 
 if __name__ == "__main__":
