@@ -30,6 +30,10 @@
 //   Only rows whose fp32 sum of squares overflowed or is tiny (< 2^-60, where
 //   squares may have underflowed) and elements outside the fp32 normal range
 //   (NaN, inf, |h*w| or |out| beyond 2^+-100) fall back to fp64.
+// The exact path runs out of line: inlined at every packed word of a thread's
+// vectors it made the kernel large enough to stall on instruction fetch (233
+// against 218 us per call on 32760 x 5120), and rows that exactly fill the CTA
+// (every width of the workloads) take a variant without bounds checks.
 // A generic kernel (any alignment or width) loops over the row twice instead
 // of keeping it in registers.
 #include "dtrot_internal.cuh"
@@ -177,17 +181,15 @@ __device__ __forceinline__ uint16_t norm_out(uint32_t hb, uint32_t wb, float inv
     return norm_out_rare(h, w, inv_hi, inv_lo);
 }
 
-__device__ __forceinline__ uint32_t norm_out2(uint32_t h2, uint32_t w2, float inv_hi,
-                                              float inv_lo) {
+// Two output elements by the exact path, out of line: the vector kernel runs it
+// for a few elements in 10^4, and inlined at each of its call sites (one per
+// packed word of a thread's vectors) it made the kernel's code large enough
+// to stall on instruction fetch.
+__device__ __noinline__ uint32_t norm_out2(uint32_t h2, uint32_t w2, float inv_hi,
+                                           float inv_lo) {
     const uint32_t lo = norm_out(h2 & 0xFFFFu, w2 & 0xFFFFu, inv_hi, inv_lo);
     const uint32_t hi = norm_out(h2 >> 16, w2 >> 16, inv_hi, inv_lo);
     return lo | (hi << 16);
-}
-
-__device__ __forceinline__ void sq_acc2(uint32_t h2, float& hi, float& lo) {
-    const float a = bf_lo(h2), b = bf_hi(h2);
-    acc_add(hi, lo, __fmul_rn(a, a));
-    acc_add(hi, lo, __fmul_rn(b, b));
 }
 
 __device__ __forceinline__ double sq_d2(uint32_t h2) {
@@ -261,8 +263,9 @@ __device__ __forceinline__ bool y_settled(float y) {
 
 // One token row on the vector path.  Thread t owns the 8-column vectors
 // v = k * blockDim + t (k < VPT, v < nv); xc, rc hold its x and residual
-// vectors of the row and wv its w vectors.
-template <int VPT>
+// vectors of the row and wv its w vectors.  FULL: nv == VPT * blockDim (every
+// thread owns VPT vectors, so no access needs a bounds check).
+template <int VPT, bool FULL>
 __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int slot, int64_t row,
                                         int nv, const uint4 (&xc)[VPT], const uint4 (&rc)[VPT],
                                         const uint4 (&wv)[VPT]) {
@@ -275,7 +278,7 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * (int)blockDim.x + tid;
-        if (v < nv) {
+        if (FULL || v < nv) {
             hv[k].x = badd2(xc[k].x, rc[k].x);
             hv[k].y = badd2(xc[k].y, rc[k].y);
             hv[k].z = badd2(xc[k].z, rc[k].z);
@@ -302,7 +305,7 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
                     const int v = k * (int)blockDim.x + tid;
-                    if (v < nv)
+                    if (FULL || v < nv)
                         d += sq_d2(hv[k].x) + sq_d2(hv[k].y) + sq_d2(hv[k].z) + sq_d2(hv[k].w);
                 }
                 return d;
@@ -320,7 +323,7 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * (int)blockDim.x + tid;
-        if (v < nv) {
+        if (FULL || v < nv) {
             const uint32_t hw[4] = {hv[k].x, hv[k].y, hv[k].z, hv[k].w};
             const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
             uint32_t o[4];
@@ -338,12 +341,12 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
     }
 }
 
-template <int VPT>
+template <int VPT, bool FULL>
 __device__ __forceinline__ void load_w(const RmsParams& p, int nv, uint4 (&wv)[VPT]) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * (int)blockDim.x + threadIdx.x;
-        if (v < nv) wv[k] = __ldg(reinterpret_cast<const uint4*>(p.w) + v);
+        if (FULL || v < nv) wv[k] = __ldg(reinterpret_cast<const uint4*>(p.w) + v);
     }
 }
 
@@ -351,22 +354,31 @@ __device__ __forceinline__ void load_w(const RmsParams& p, int nv, uint4 (&wv)[V
 // C <= 8 * VPT * blockDim.  Persistent CTAs, one token row at a time;
 // each thread keeps its w vectors in registers for the whole launch and
 // prefetches the next row's x and residual vectors into registers while it
-// works on the current row.
-template <int VPT>
-__global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
+// works on the current row.  Register budgets: the launcher gives VPT 2 and 4
+// at most 160 threads, and the bounds below keep 5 and 3 such CTAs per SM
+// (unbounded, the guard-free FULL variant of VPT 2 took 118 registers and fit
+// 3, 5% slower at C = 2560; bounding VPT 1 the same way made C = 768 6%
+// slower, so VPT 1 and 8 keep the compiler's choice: a minimum of 0 CTAs
+// leaves the register count unconstrained).
+constexpr int rms_max_threads(int vpt) { return (vpt == 2 || vpt == 4) ? 160 : 256; }
+constexpr int rms_min_blocks(int vpt) { return vpt == 2 ? 5 : vpt == 4 ? 3 : 0; }
+
+template <int VPT, bool FULL>
+__global__ void __launch_bounds__(rms_max_threads(VPT), rms_min_blocks(VPT))
+    rms_vec_kernel(RmsParams p) {
     __shared__ RowShared sh;
     pdl_wait();
     const int nv = (int)(p.C >> 3);
     const int tid = threadIdx.x;
     uint4 wv[VPT], xc[VPT], rc[VPT];
-    load_w<VPT>(p, nv, wv);
+    load_w<VPT, FULL>(p, nv, wv);
     auto load_row = [&](int64_t r, uint4 (&xs)[VPT], uint4 (&rs)[VPT]) {
         const uint4* xr = reinterpret_cast<const uint4*>(p.x + r * p.sx);
         const uint4* rr = reinterpret_cast<const uint4*>(p.residual + r * p.sr);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * (int)blockDim.x + tid;
-            if (v < nv) {
+            if (FULL || v < nv) {
                 xs[k] = xr[v];
                 rs[k] = rr[v];
             }
@@ -379,7 +391,7 @@ __global__ void __launch_bounds__(256) rms_vec_kernel(RmsParams p) {
         uint4 xn[VPT], rn[VPT];
         const int64_t nrow = row + gridDim.x;
         if (nrow < p.T) load_row(nrow, xn, rn);
-        rms_row<VPT>(p, sh, slot, row, nv, xc, rc, wv);
+        rms_row<VPT, FULL>(p, sh, slot, row, nv, xc, rc, wv);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             xc[k] = xn[k];
@@ -432,15 +444,22 @@ cudaError_t per_sm_blocks(K kernel, int threads, size_t smem, int* n) {
     return e;
 }
 
-template <int VPT>
-cudaError_t launch_vec(const RmsParams& p, int threads, cudaStream_t st) {
+template <int VPT, bool FULL>
+cudaError_t launch_vec_as(const RmsParams& p, int threads, cudaStream_t st) {
     // persistent grid: as many CTAs as fit on the device at once, at most T
     int per_sm = 0;
-    cudaError_t e = per_sm_blocks(rms_vec_kernel<VPT>, threads, 0, &per_sm);
+    cudaError_t e = per_sm_blocks(rms_vec_kernel<VPT, FULL>, threads, 0, &per_sm);
     if (e != cudaSuccess) return e;
     int64_t blocks = (int64_t)num_sms() * per_sm;
     if (blocks > p.T) blocks = p.T;
-    return launch_pdl(rms_vec_kernel<VPT>, dim3((unsigned)blocks), dim3(threads), 0, st, p);
+    return launch_pdl(rms_vec_kernel<VPT, FULL>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                      p);
+}
+
+template <int VPT>
+cudaError_t launch_vec(const RmsParams& p, int threads, cudaStream_t st) {
+    return (p.C / 8 == (int64_t)VPT * threads) ? launch_vec_as<VPT, true>(p, threads, st)
+                                               : launch_vec_as<VPT, false>(p, threads, st);
 }
 
 }  // namespace
