@@ -707,7 +707,7 @@ def native(args):
         "config": config_for(wl, per_step, f"replicas x{world}"),
         "pct_of_peak": round(100 * value / world / peak, 2),
         # the same against the part's nominal HBM3e bandwidth (7.7 TB/s, "~8 TB/s");
-        # the >= 80% target is judged against the measured copy peak above (the
+        # the >= 80% target is stated against the measured copy peak above (the
         # nominal figure is the fallback only where no measured one exists)
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         # B*S over the layer's ops (the tables are once per forward), per-op times
