@@ -14,7 +14,10 @@
  *  - `stream` is a cudaStream_t passed as `void*`; NULL means the legacy
  *    default stream.  Work is enqueued on it and the call returns without
  *    synchronising.  The library allocates nothing, frees nothing and makes no
- *    host-device synchronisation, so calls may be captured in a CUDA graph.
+ *    host-device synchronisation, so the compute calls may be captured in a
+ *    CUDA graph (the one exception is dtrot_gemm_gelu_and_mul_error, which
+ *    copies a word to host memory and waits for it when that memory is
+ *    pageable).
  *  - Each kernel is launched as a programmatic dependent of the work before it
  *    in the stream (so its launch overlaps the end of that work) and waits for
  *    that work to complete before it reads or writes any memory: the memory
