@@ -15,9 +15,9 @@
  *    default stream.  Work is enqueued on it and the call returns without
  *    synchronising.  The library allocates nothing, frees nothing and makes no
  *    host-device synchronisation, so the compute calls may be captured in a
- *    CUDA graph (the one exception is dtrot_gemm_gelu_and_mul_error, which
- *    copies a word to host memory and waits for it when that memory is
- *    pageable).
+ *    CUDA graph (dtrot_gelu_and_mul_noalloc aside: see its notes below).
+ *    dtrot_gemm_gelu_and_mul_error is the one call that copies to host
+ *    memory, and it waits for the copy when that memory is pageable.
  *  - Each kernel is launched as a programmatic dependent of the work before it
  *    in the stream (so its launch overlaps the end of that work) and waits for
  *    that work to complete before it reads or writes any memory: the memory
