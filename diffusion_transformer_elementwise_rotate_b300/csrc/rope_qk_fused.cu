@@ -20,9 +20,10 @@
 //     issued before any of its stores; the first batch is loaded before the
 //     token's cos/sin row is fetched or evaluated;
 //   - with angles, the warp first evaluates the token's rot_dim (cos, sin)
-//     pairs, one column per lane at a time, into its slot of shared memory and
-//     then reads its vectors from there; the same registers serve every q and
-//     k head of the token;
+//     pairs, one first-half column and its second-half partner per lane at a
+//     time (the partner's entry copied when its angle has the same bits),
+//     into its slot of shared memory and then reads its vectors from there;
+//     the same registers serve every q and k head of the token;
 //   - tail columns [rot_dim, D) are not touched: in place they already hold x.
 // Generic path: one thread per (token, head row of q or k, pair index).
 #include "dtrot_internal.cuh"
@@ -122,12 +123,24 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
         load_batch(ri);
         V c1, c2, s1, s2;
         if constexpr (ANGLES) {
+            // column c of the first half and its partner c + hh: a partner
+            // angle with the same bits has the same entry, which is copied
+            // (per-axis rotate-half angles repeat their half-row); any other
+            // is evaluated
             const float* fr = p.freqs + (s * p.B + b) * p.rot;
-            for (int64_t c = lane; c < p.rot; c += 32) {
+            for (int64_t c = lane; c < hh; c += 32) {
+                const float f1 = __ldg(fr + c), f2 = __ldg(fr + c + hh);
                 uint16_t cv, sv;
-                cos_sin_entry(__ldg(fr + c), cv, sv);
+                cos_sin_entry(f1, cv, sv);
                 cs[w][0][c] = cv;
                 cs[w][1][c] = sv;
+                if (__float_as_uint(f2) != __float_as_uint(f1)) {
+                    const uint32_t e = cos_sin_entry_call(f2);
+                    cv = (uint16_t)e;
+                    sv = (uint16_t)(e >> 16);
+                }
+                cs[w][0][c + hh] = cv;
+                cs[w][1][c + hh] = sv;
             }
             __syncwarp();
             if (active) {

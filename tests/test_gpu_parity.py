@@ -281,6 +281,24 @@ def test_rope_qk_special_angles_match_the_table_kernel():
     _qk_check(1, 64, 2, 2, 32, 32, freqs, 10, "angles")
 
 
+def test_rope_qk_angles_second_half_reused_only_for_identical_bits():
+    # angle mode evaluates column j of the first half and copies the entry to
+    # j + rot/2 when that angle has the same bits: equal halves, one column off,
+    # +0 against -0, NaN payloads, and random halves, checked against the
+    # oracle's tables
+    g = torch.Generator().manual_seed(31)
+    S, B, R = 131, 2, 64
+    f = torch.rand((S, B, 1, R), generator=g) * 400.0 - 200.0
+    f[: S // 2, :, :, R // 2:] = f[: S // 2, :, :, : R // 2]
+    f[1::5, :, :, R // 2 + 3] += 1.0
+    f[2, 0, 0, 5], f[2, 0, 0, R // 2 + 5] = 0.0, -0.0
+    f[3, 1, 0, 6], f[3, 1, 0, R // 2 + 6] = -0.0, 0.0
+    nan_a = np.array([0x7FC00001], dtype=np.uint32).view(np.float32)[0]
+    nan_b = np.array([0xFFC00002], dtype=np.uint32).view(np.float32)[0]
+    f[4, 0, 0, 1], f[4, 0, 0, R // 2 + 1] = float(nan_a), float(nan_b)
+    _qk_check(B, S, 3, 2, R, R, f.contiguous(), 77, "angles")
+
+
 def test_rope_qk_video_full_size_sampled_tokens():
     wl = W.WORKLOADS["video"]
     q, k = W.rope_inputs(wl, "q"), W.rope_inputs(wl, "k")
