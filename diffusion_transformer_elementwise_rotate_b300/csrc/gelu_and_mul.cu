@@ -7,12 +7,13 @@
 //
 // Design.  gate is bf16, so the rounded activation g(gate) takes one of 65536
 // values.  A first kernel tabulates g for every bf16 bit pattern into a
-// 128 KB workspace, one entry per thread over the whole GPU.  The streaming
-// kernel is launched as its programmatic dependent: its persistent CTAs (one
-// per SM) start while the table kernel drains, wait for it in hardware
-// (griddepcontrol.wait), copy the table into shared memory and stream gate/up
-// with 128-bit loads: per element one shared-memory lookup and one bf16x2
-// multiply with .rn rounding.  The erf arithmetic (tens of fp32 instructions
+// 128 KB workspace, one entry per thread over the whole GPU; it evaluates its
+// entry before waiting for the kernel before it, and only the store waits.
+// The streaming kernel is launched as its programmatic dependent: its
+// persistent CTAs (one per SM) are scheduled as the table kernel's CTAs exit,
+// wait for it in hardware (griddepcontrol.wait), copy the table into shared
+// memory and stream gate/up with 128-bit loads: per element one shared-memory
+// lookup and one bf16x2 multiply with .rn rounding.  The erf arithmetic (tens of fp32 instructions
 // per element, enough to make a direct evaluation ALU-bound on this part) is
 // paid 65536 times per call instead of once per element, and the result is
 // the exactly rounded GELU.
