@@ -127,12 +127,37 @@ def step_bytes(wl, W):
     }
 
 
+def code_text(src: str) -> str:
+    """C/C++ source without its comments and with whitespace collapsed, so that
+    a comment edit does not count as a change of the kernel."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif src[i] == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash(*names: str) -> str:
-    """sha256 prefix of the named csrc files, concatenated in order."""
+    """sha256 prefix of the code (comments stripped) of the named csrc files,
+    concatenated in order."""
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(ROOT, PKG, "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, PKG, "csrc", name), encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
