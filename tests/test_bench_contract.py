@@ -46,3 +46,13 @@ def test_reference_arm_other_ranks_exit_without_work():
              "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3")
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_source_hash_ignores_comments_and_whitespace():
+    import bench
+    a = 'int f(int x) { // doubles\n  return 2 * x; /* fast */ }\nconst char* s = "// kept";\n'
+    b = 'int f(int x) {\n    return 2 * x;   }\n   const char* s = "// kept";'
+    c = 'int f(int x) { return 3 * x; } const char* s = "// kept";'
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
+    assert '"// kept"' in bench.code_text(a)
