@@ -747,3 +747,37 @@ def test_rope_2_14_elements(D, rot, S):
     assert_bitexact(_rope_case(x, cos_b, sin_b), exp, f"S={S} H={H} D={D} rot={rot}")
     for mode in ("tables", "angles"):
         _qk_check(B, S, H, max(1, H // 4), D, rot, freqs, 330 + D + rot + S, mode)
+
+
+# ---------------------------------------------------------------- degenerate sizes
+
+@pytest.mark.parametrize("B,S,H,D,rot", [(1, 1, 1, 2, 2), (2, 3, 1, 8, 2), (1, 5, 3, 6, 4),
+                                         (1, 7, 2, 16, 16), (3, 1, 5, 10, 6)])
+def test_rope_smallest_shapes(B, S, H, D, rot):
+    # one or two pair columns, heads of 2-16 columns, a single token: the
+    # generic and narrow-vector paths, the tables and both q+k modes
+    x = W.normal_bf16((B, S, H, D), 400 + D + rot, 0)
+    freqs = W.freqs_1d(S, B, rot)
+    cos_b, sin_b = oracle.rope_cos_sin(freqs.numpy())
+    gc, gs = dt.rope_cos_sin_precompute(to_dev(freqs))
+    torch.cuda.synchronize()
+    assert_bitexact(bits(gc), cos_b, "cos")
+    assert_bitexact(bits(gs), sin_b, "sin")
+    exp = oracle.rope_rotate_half(bits(x), cos_b, sin_b)
+    assert_bitexact(_rope_case(x, cos_b, sin_b), exp, f"B={B} S={S} H={H} D={D} rot={rot}")
+    for mode in ("tables", "angles"):
+        _qk_check(B, S, H, 1, D, rot, freqs, 410 + D + rot, mode, layout="separate")
+
+
+@pytest.mark.parametrize("T,F", [(1, 1), (3, 1), (1, 8), (2, 9), (1, 1001)])
+def test_geglu_smallest_shapes(T, F):
+    gu = W.normal_bf16((T, 2 * F), 420 + T + F, 2)
+    _geglu_check(gu, F, None, f"T={T} F={F}")
+
+
+@pytest.mark.parametrize("T,C", [(1, 8), (1, 2), (2, 1), (1, 5120), (3, 16)])
+def test_rmsnorm_smallest_shapes(T, C):
+    x = W.normal_bf16((T, C), 430 + T + C, 4)
+    r = W.normal_bf16((T, C), 430 + T + C, 5, std=2.0)
+    w = W.normal_bf16((C,), 430 + T + C, 6, mean=1.0, std=0.316)
+    _rms_check(x, r, w, None, f"T={T} C={C}")
