@@ -289,9 +289,7 @@ class Layer:
             dt.gelu_and_mul(gate, up, out=d["ff_out"])
         else:
             st = torch.cuda.current_stream(gate.device).cuda_stream
-            ws = dt.gelu_workspace(gate.device, st)
-            nbytes = ws.numel() * ws.element_size()
-            dt._capi.check("dtrot_gelu_table_build", ws.data_ptr(), nbytes, st)
+            ws = dt.gelu_table_build(dt.gelu_workspace(gate.device, st))
             geglu_kernel_ev.record()
             dt.gelu_and_mul(gate, up, out=d["ff_out"], table=ws)
         mark(4)

@@ -6,8 +6,8 @@ RMSNorm fused with the residual add.  The torch wrappers in `api` only pass
 pointers, sizes and strides; `_capi` is the raw ctypes binding.
 """
 from . import selfcheck  # noqa: F401
-from ._capi import DtrotError, DtrotUnavailable, load  # noqa: F401
-from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_table, gelu_workspace,  # noqa: F401
-                  gemm_gelu_and_mul,
+from ._capi import DtrotError, DtrotKernelError, DtrotUnavailable, load  # noqa: F401
+from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_table, gelu_table_build,  # noqa: F401
+                  gelu_workspace, gemm_error_word, gemm_gelu_and_mul,
                   rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half,
                   rope_rotate_half_qk_)

@@ -11,6 +11,7 @@ runs in libdtrot's sm_103a kernels.
                                          tables, or angles evaluated in the kernel
   gelu_and_mul(gate, up, out=None, workspace=None, table=None) -> out   ERNIE-Image page, section 3
   gelu_table(device)                      -> the activation table, built once per device
+  gelu_table_build(table)                 -> fills a caller buffer with the activation table
   gelu_and_mul_fused(gate_up, out=None)   -> out         (gate = first half of the last dim)
   gemm_gelu_and_mul(x, w, out=None, workspace=None, check=False) -> out   GEGLU in the
                                          epilogue of the gate_up projection x w^T (tcgen05
@@ -178,6 +179,19 @@ def gelu_workspace(device: torch.device, stream: int) -> torch.Tensor:
 
 
 _tables: dict = {}
+
+
+def gelu_table_build(table: torch.Tensor) -> torch.Tensor:
+    """Fill `table` (a CUDA buffer of at least dtrot_gelu_and_mul_workspace_bytes()
+    bytes, 16-byte aligned) with the GEGLU activation table on the current
+    stream; gelu_and_mul(..., table=table) then runs the streaming kernel
+    alone.  gelu_and_mul(gate, up, workspace=ws) is this followed by
+    gelu_and_mul(gate, up, table=ws)."""
+    if not isinstance(table, torch.Tensor) or not table.is_cuda:
+        raise ValueError("table must be a CUDA tensor")
+    _capi.check("dtrot_gelu_table_build", table.data_ptr(),
+                table.numel() * table.element_size(), _stream(table))
+    return table
 
 
 def gelu_table(device) -> torch.Tensor:

@@ -781,3 +781,18 @@ def test_rmsnorm_smallest_shapes(T, C):
     r = W.normal_bf16((T, C), 430 + T + C, 5, std=2.0)
     w = W.normal_bf16((C,), 430 + T + C, 6, mean=1.0, std=0.316)
     _rms_check(x, r, w, None, f"T={T} C={C}")
+
+
+def test_geglu_table_built_into_a_caller_buffer():
+    # gelu_table_build + gelu_and_mul(table=) are the two halves of the
+    # self-contained call; every gate value through them against the oracle
+    from diffusion_transformer_elementwise_rotate_b300 import _capi
+    n = int(_capi.load().dtrot_gelu_and_mul_workspace_bytes())
+    buf = torch.full((n,), 0xA5, dtype=torch.uint8, device=DEV)   # stale contents
+    dt.gelu_table_build(buf)
+    gate = torch.from_numpy(np.arange(1 << 16, dtype=np.uint16).view(np.int16)).view(
+        torch.bfloat16).view(64, 1024)
+    up = W.normal_bf16((64, 1024), 440, 3)
+    out = dt.gelu_and_mul(to_dev(gate), to_dev(up), table=buf)
+    torch.cuda.synchronize()
+    assert_bitexact(bits(out), oracle.gelu_and_mul(bits(gate), bits(up)), "table in a buffer")
