@@ -796,3 +796,57 @@ def test_geglu_table_built_into_a_caller_buffer():
     out = dt.gelu_and_mul(to_dev(gate), to_dev(up), table=buf)
     torch.cuda.synchronize()
     assert_bitexact(bits(out), oracle.gelu_and_mul(bits(gate), bits(up)), "table in a buffer")
+
+
+def test_concurrent_callers_on_their_own_streams():
+    # four host threads, each on its own stream, run GEGLU (each stream gets its
+    # own workspace), RMSNorm and RoPE at once; the library's per-device caches
+    # are filled concurrently.  Every result must match the oracle.
+    import threading
+    wl = W.WORKLOADS["tiny"]
+    freqs = W.freqs_for(wl)
+    ec, es = oracle.rope_cos_sin(freqs.numpy())
+    cases = []
+    for i in range(4):
+        gu = W.normal_bf16((257, 2 * 520), 600 + i, 2)
+        x = W.normal_bf16((129, 768), 600 + i, 4)
+        r = W.normal_bf16((129, 768), 600 + i, 5, std=2.0)
+        w = W.normal_bf16((768,), 600 + i, 6, mean=1.0, std=0.316)
+        q = W.normal_bf16((1, 256, 4, 64), 600 + i, 0)
+        cases.append((gu, x, r, w, q))
+    results = [None] * 4
+    errors = []
+    barrier = threading.Barrier(4)
+
+    def work(i):
+        try:
+            gu, x, r, w, q = cases[i]
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                dgu, dx, dr, dw, dq = (to_dev(t) for t in (gu, x, r, w, q))
+                c, s = dt.rope_cos_sin_precompute(to_dev(freqs))
+                barrier.wait()
+                for _ in range(5):
+                    ff = dt.gelu_and_mul_fused(dgu)
+                    rr = dr.clone()
+                    y = dt.rmsnorm_residual(dx, rr, dw, EPS)
+                    qo = dt.rope_rotate_half(dq, c, s)
+            st.synchronize()
+            results[i] = (bits(ff), bits(rr), bits(y), bits(qo))
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, (gu, x, r, w, q) in enumerate(cases):
+        ff, rr, y, qo = results[i]
+        g = bits(gu)
+        assert_bitexact(ff, oracle.gelu_and_mul(g[:, :520], g[:, 520:]), f"thread {i} geglu")
+        h, ye = oracle.rmsnorm_residual(bits(x), bits(r), bits(w), EPS)
+        assert_bitexact(rr, h, f"thread {i} residual")
+        assert_within_tolerance(y, ye, f"thread {i} rmsnorm")
+        assert_bitexact(qo, oracle.rope_rotate_half(bits(q), ec, es), f"thread {i} rope")
