@@ -299,12 +299,17 @@ def test_rope_qk_angles_second_half_reused_only_for_identical_bits():
     _qk_check(B, S, 3, 2, R, R, f.contiguous(), 77, "angles")
 
 
-def test_rope_qk_video_full_size_sampled_tokens():
+@pytest.mark.parametrize("mode", ["angles", "tables"])
+def test_rope_qk_video_full_size_sampled_tokens(mode):
     wl = W.WORKLOADS["video"]
     q, k = W.rope_inputs(wl, "q"), W.rope_inputs(wl, "k")
     freqs = W.freqs_for(wl)
     dq, dk = to_dev(q), to_dev(k)
-    dt.rope_rotate_half_qk_(dq, dk, freqs=to_dev(freqs))
+    if mode == "angles":
+        dt.rope_rotate_half_qk_(dq, dk, freqs=to_dev(freqs))
+    else:
+        c, s = dt.rope_cos_sin_precompute(to_dev(freqs))
+        dt.rope_rotate_half_qk_(dq, dk, cos=c, sin=s)
     torch.cuda.synchronize()
     rng = np.random.default_rng(4)
     toks = np.unique(np.concatenate([[0, wl.S - 1], rng.choice(wl.S, 512, replace=False)]))
