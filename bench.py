@@ -564,10 +564,36 @@ def fused_mlp_geglu(dt, layer, wl, reps):
                 "fused_over_matmul": round(ms_fused / ms_mm, 4)}}
 
 
+def oracle_sample_inputs(oracle, h, tok, rows_ff, rows_n):
+    """The oracle's inputs for a sample of a layer: the first `tok` positions
+    of the angles and of q and k, the first `rows_ff` GEGLU rows and the first
+    `rows_n` rows of each RMSNorm, as bf16 bit arrays, cut from the layer's
+    host inputs `h`."""
+    b = oracle.bf16_bits
+    return {"freqs": h["freqs"][:tok].numpy(), "q": b(h["q"][:, :tok]), "k": b(h["k"][:, :tok]),
+            "gate_up": b(h["gate_up"][:rows_ff]),
+            "x1": b(h["x1"][:rows_n]), "r1": b(h["r1"][:rows_n]),
+            "x2": b(h["x2"][:rows_n]), "r2": b(h["r2"][:rows_n]), "w": b(h["w"])}
+
+
+def oracle_step(oracle, inp, F):
+    """One pass of the whole path in the oracle, the outputs named like the
+    layer's device outputs (r1 and r2: the updated residual streams)."""
+    c, s = oracle.rope_cos_sin(inp["freqs"])
+    gu = inp["gate_up"]
+    h1, y1 = oracle.rmsnorm_residual(inp["x1"], inp["r1"], inp["w"], 1e-6)
+    h2, y2 = oracle.rmsnorm_residual(inp["x2"], inp["r2"], inp["w"], 1e-6)
+    return {"cos": c, "sin": s,
+            "q_out": oracle.rope_rotate_half(inp["q"], c, s),
+            "k_out": oracle.rope_rotate_half(inp["k"], c, s),
+            "ff_out": oracle.gelu_and_mul(gu[:, :F], gu[:, F:]),
+            "y1": y1, "y2": y2, "r1": h1, "r2": h2}
+
+
 def cpu_baseline(wl, W, layer, target_s=15.0):
     """Time the oracle (as it stands, all host cores it uses) on a bounded
-    sample of the same workload: the first `frac` of each op's rows."""
-    import numpy as np
+    sample of the same workload: the first `frac` of each op's rows.  The
+    outputs of the multi-core sample are then checked against the GPU's."""
     sys.path.insert(0, ROOT)
     import oracle
     h = layer.h_in
@@ -578,27 +604,19 @@ def cpu_baseline(wl, W, layer, target_s=15.0):
         tok = max(1, int(wl.S * frac))
         rows_ff = max(1, int(wl.T_ff * frac))
         rows_n = max(1, int(wl.T_norm * frac))
-        F = wl.F
-        freqs = h["freqs"][:tok].numpy()
-        q = oracle.bf16_bits(h["q"][:, :tok])
-        k = oracle.bf16_bits(h["k"][:, :tok])
-        gu = oracle.bf16_bits(h["gate_up"][:rows_ff])
-        x1, r1 = oracle.bf16_bits(h["x1"][:rows_n]), oracle.bf16_bits(h["r1"][:rows_n])
-        x2, r2 = oracle.bf16_bits(h["x2"][:rows_n]), oracle.bf16_bits(h["r2"][:rows_n])
-        w = oracle.bf16_bits(h["w"])
+        inp = oracle_sample_inputs(oracle, h, tok, rows_ff, rows_n)
         t0 = time.perf_counter()
-        c, s = oracle.rope_cos_sin(freqs)
-        oracle.rope_rotate_half(q, c, s)
-        oracle.rope_rotate_half(k, c, s)
-        oracle.gelu_and_mul(gu[:, :F], gu[:, F:])
-        oracle.rmsnorm_residual(x1, r1, w, 1e-6)
-        oracle.rmsnorm_residual(x2, r2, w, 1e-6)
+        out = oracle_step(oracle, inp, wl.F)
         dt_s = time.perf_counter() - t0
+        last.clear()
+        last.update(out)
         sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S
                    + 2 * bts["rope_rotate_half_q"] * tok / wl.S
                    + bts["gelu_and_mul"] * rows_ff / wl.T_ff
                    + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
         return dt_s, sampled, (tok, rows_ff, rows_n)
+
+    last = {}
 
     def fill(frac, target):
         """Rescale the sample until one run takes at least half of `target`."""
@@ -610,6 +628,7 @@ def cpu_baseline(wl, W, layer, target_s=15.0):
 
     run(1.0 / 2048)  # warm-up (thread pool start-up)
     t, sampled, (tok, rf, rn) = fill(1.0 / 256, target_s)
+    parity = sample_parity(last, layer, wl, tok, rf, rn) if layer.h_out else None
     # one core, on a sample a few seconds long (rows are independent, so the
     # rate carries over to the whole layer)
     cores = oracle.num_threads()
@@ -628,7 +647,48 @@ def cpu_baseline(wl, W, layer, target_s=15.0):
                        f"RoPE, first {rf} of {wl.T_ff} GEGLU rows, first {rn} of {wl.T_norm} "
                        f"rows for each RMSNorm; {sampled / 1e9:.3f} GB of algorithmic traffic "
                        f"in {t:.2f} s"),
-            "fraction_of_step": round(sampled / total_bytes, 6)}
+            "fraction_of_step": round(sampled / total_bytes, 6),
+            "parity": parity}
+
+
+def _ordered(bits):
+    """bf16 bit patterns -> integers in value order (+0 and -0 both 0), so
+    that a difference counts units in the last place."""
+    import numpy as np
+    v = bits.astype(np.int32)
+    m = v & 0x7FFF
+    return np.where(v & 0x8000, -m, m)
+
+
+def sample_parity(ref, layer, wl, tok, rows_ff, rows_n):
+    """The oracle's outputs on the CPU sample against the same rows of the
+    GPU's outputs from the last end-to-end step (all inputs uploaded from the
+    host copies the sample is cut from, all outputs downloaded), element by
+    element: per output, the elements compared, how many differ in their bits
+    and the largest difference in bf16 ulps."""
+    import numpy as np
+    import oracle
+    B, S, R = wl.B, wl.S, wl.rot
+    gpu = {n: oracle.bf16_bits(t) for n, t in layer.h_out.items()}
+    cut = {"cos": gpu["cos"].reshape(B, S, R)[:, :tok].reshape(B * tok, R),
+           "sin": gpu["sin"].reshape(B, S, R)[:, :tok].reshape(B * tok, R),
+           "q_out": gpu["q_out"][:, :tok], "k_out": gpu["k_out"][:, :tok],
+           "ff_out": gpu["ff_out"][:rows_ff]}
+    for n in ("y1", "y2", "r1", "r2"):
+        cut[n] = gpu[n][:rows_n]
+    res, exact = {}, True
+    for n, want in ref.items():
+        got = cut[n]
+        if got.shape != want.shape:
+            raise RuntimeError(f"sample parity: {n} shapes {got.shape} vs {want.shape}")
+        diff = int(np.count_nonzero(got != want))
+        ulp = int(np.abs(_ordered(got) - _ordered(want)).max()) if want.size else 0
+        res[n] = {"elements": int(want.size), "differing": diff, "max_ulp": ulp}
+        exact = exact and diff == 0
+    return {"bit_exact": exact, "outputs": res,
+            "how": ("the GPU outputs of the last end-to-end step (inputs uploaded from the host "
+                    "copies, outputs downloaded) against the oracle on the sample above, "
+                    "element by element")}
 
 
 def native(args):

@@ -56,3 +56,42 @@ def test_source_hash_ignores_comments_and_whitespace():
     assert bench.code_text(a) == bench.code_text(b)
     assert bench.code_text(a) != bench.code_text(c)
     assert '"// kept"' in bench.code_text(a)
+
+
+def test_sample_parity_checks_the_sampled_rows():
+    """The benchmark's check of the GPU outputs against the oracle on its CPU
+    sample, run here on outputs the oracle made for the whole layer: they
+    agree; one bit flipped inside the sample is counted, one outside it is not.
+    B = 2 puts the second sequence's table rows at S + s in the layer and at
+    tok + s in the sample."""
+    import dataclasses
+
+    import torch
+
+    import oracle
+    from diffusion_transformer_elementwise_rotate_b300 import workloads as W
+    wl = dataclasses.replace(W.WORKLOADS["tiny"], name="tiny_b2", B=2, S=64, grid=(64,),
+                             T_ff=48, T_norm=40)
+    layer = bench.Layer(wl, W, torch.device("cpu"))
+    full = bench.oracle_step(
+        oracle, bench.oracle_sample_inputs(oracle, layer.h_in, wl.S, wl.T_ff, wl.T_norm), wl.F)
+    assert set(full) == set(layer.out_names)
+    for n, a in full.items():
+        layer.h_out[n].copy_(oracle.from_bits(a).reshape(layer.h_out[n].shape))
+    tok, rf, rn = 16, 20, 10
+    ref = bench.oracle_step(oracle, bench.oracle_sample_inputs(oracle, layer.h_in, tok, rf, rn),
+                            wl.F)
+    res = bench.sample_parity(ref, layer, wl, tok, rf, rn)
+    assert res["bit_exact"]
+    assert res["outputs"]["cos"]["elements"] == wl.B * tok * wl.rot
+    assert res["outputs"]["q_out"]["elements"] == wl.B * tok * wl.H * wl.D
+    assert res["outputs"]["ff_out"]["elements"] == rf * wl.F
+    assert res["outputs"]["y2"]["elements"] == rn * wl.C
+    layer.h_out["cos"].view(torch.int16)[wl.S + 3, 5] ^= 1      # b = 1, s = 3: sampled
+    layer.h_out["ff_out"].view(torch.int16)[rf + 1, 0] ^= 1     # beyond the sampled rows
+    layer.h_out["k_out"].view(torch.int16)[1, tok, 0, 0] ^= 1   # position tok: not sampled
+    res = bench.sample_parity(ref, layer, wl, tok, rf, rn)
+    assert not res["bit_exact"]
+    diff = {n: o["differing"] for n, o in res["outputs"].items()}
+    assert diff == {n: int(n == "cos") for n in layer.out_names}
+    assert res["outputs"]["cos"]["max_ulp"] == 1
