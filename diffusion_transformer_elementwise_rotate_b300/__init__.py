@@ -10,4 +10,4 @@ from ._capi import DtrotError, DtrotKernelError, DtrotUnavailable, load  # noqa:
 from .api import (gelu_and_mul, gelu_and_mul_fused, gelu_table, gelu_table_build,  # noqa: F401
                   gelu_workspace, gemm_error_word, gemm_gelu_and_mul,
                   rmsnorm_residual, rope_cos_sin_precompute, rope_rotate_half,
-                  rope_rotate_half_qk_)
+                  rope_rotate_half_qk, rope_rotate_half_qk_)

@@ -41,6 +41,10 @@ SIGNATURES = {
     "dtrot_rope_rotate_half_qk": (ctypes.c_int, [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64,
                                                   _i64, _i64, _i64, _i64, _i64, _p, _p, _p,
                                                   _i64, _p]),
+    "dtrot_rope_rotate_half_qk_out": (ctypes.c_int, [_p, _i64, _i64, _i64, _i64, _p, _i64,
+                                                      _i64, _i64, _i64, _i64, _i64, _i64, _p,
+                                                      _p, _p, _i64, _p, _i64, _i64, _i64, _p,
+                                                      _i64, _i64, _i64, _p]),
     "dtrot_gelu_and_mul_workspace_bytes": (ctypes.c_int64, []),
     "dtrot_gelu_and_mul": (ctypes.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i64, _p, _i64,
                                           _p]),

@@ -110,13 +110,10 @@ def rope_rotate_half(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
     return out
 
 
-def rope_rotate_half_qk_(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | None = None,
-                         sin: torch.Tensor | None = None,
-                         freqs: torch.Tensor | None = None) -> None:
-    """Rotates q (B, S, Hq, D) and k (B, S, Hk, D) in place with one launch.
-    Give either the cos/sin tables (bf16 (B*S, rot)) or the angles `freqs`
-    (fp32 (S, B, 1, rot)), from which the kernel evaluates the rows itself.
-    q and k may be the q and k head ranges of one fused QKV tensor."""
+def _qk_args(q, k, cos, sin, freqs):
+    """Shapes of a q+k RoPE call and the pointers of its tables or angles:
+    (B, S, Hq, Hk, D, rot, cos_ptr, sin_ptr, freqs_ptr), 0 for a pointer not
+    given."""
     _need(q, "q", torch.bfloat16)
     _need(k, "k", torch.bfloat16)
     if q.dim() != 4 or k.dim() != 4:
@@ -133,18 +130,33 @@ def rope_rotate_half_qk_(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | N
         _need(freqs, "freqs", torch.float32)
         if freqs.dim() != 4 or freqs.shape[:3] != (S, B, 1) or not freqs.is_contiguous():
             raise ValueError("freqs must be contiguous (S, B, 1, rot)")
-        rot = freqs.shape[3]
-        cp = sp = 0
-        fp = freqs.data_ptr()
-    else:
-        _need(cos, "cos", torch.bfloat16)
-        _need(sin, "sin", torch.bfloat16)
-        if cos.dim() != 2 or cos.shape != sin.shape or cos.shape[0] != B * S:
-            raise ValueError("cos/sin must be (B*S, rot_dim)")
-        if not (cos.is_contiguous() and sin.is_contiguous()):
-            raise ValueError("cos/sin must be contiguous")
-        rot = cos.shape[1]
-        cp, sp, fp = cos.data_ptr(), sin.data_ptr(), 0
+        return B, S, Hq, Hk, D, freqs.shape[3], 0, 0, freqs.data_ptr()
+    _need(cos, "cos", torch.bfloat16)
+    _need(sin, "sin", torch.bfloat16)
+    if cos.dim() != 2 or cos.shape != sin.shape or cos.shape[0] != B * S:
+        raise ValueError("cos/sin must be (B*S, rot_dim)")
+    if not (cos.is_contiguous() and sin.is_contiguous()):
+        raise ValueError("cos/sin must be contiguous")
+    return B, S, Hq, Hk, D, cos.shape[1], cos.data_ptr(), sin.data_ptr(), 0
+
+
+def _qk_selfcheck(pairs, cos, sin, freqs):
+    """First-call check of a q+k RoPE call: each (name, input copy, output)
+    against the plain torch reference."""
+    if freqs is not None:
+        cos, sin = _sc.ref_tables(freqs)
+    for name, x0, out in pairs:
+        _sc.compare(name, out, _sc.ref_rope(x0, cos, sin), exact=True)
+
+
+def rope_rotate_half_qk_(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | None = None,
+                         sin: torch.Tensor | None = None,
+                         freqs: torch.Tensor | None = None) -> None:
+    """Rotates q (B, S, Hq, D) and k (B, S, Hk, D) in place with one launch.
+    Give either the cos/sin tables (bf16 (B*S, rot)) or the angles `freqs`
+    (fp32 (S, B, 1, rot)), from which the kernel evaluates the rows itself.
+    q and k may be the q and k head ranges of one fused QKV tensor."""
+    B, S, Hq, Hk, D, rot, cp, sp, fp = _qk_args(q, k, cos, sin, freqs)
     sq, sk = q.stride(), k.stride()
     key = _sc.want("rope_rotate_half_qk", q, k, cos if freqs is None else freqs)
     q0, k0 = (q.clone(), k.clone()) if key else (None, None)
@@ -152,10 +164,39 @@ def rope_rotate_half_qk_(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | N
                 k.data_ptr(), Hk, sk[0], sk[1], sk[2], B, S, D, cp or None, sp or None,
                 fp or None, rot, _stream(q))
     if key:
-        if freqs is not None:
-            cos, sin = _sc.ref_tables(freqs)
-        _sc.compare("rope_rotate_half_qk q", q, _sc.ref_rope(q0, cos, sin), exact=True)
-        _sc.compare("rope_rotate_half_qk k", k, _sc.ref_rope(k0, cos, sin), exact=True)
+        _qk_selfcheck([("rope_rotate_half_qk q", q0, q), ("rope_rotate_half_qk k", k0, k)],
+                      cos, sin, freqs)
+
+
+def rope_rotate_half_qk(q: torch.Tensor, k: torch.Tensor, cos: torch.Tensor | None = None,
+                        sin: torch.Tensor | None = None, freqs: torch.Tensor | None = None,
+                        q_out: torch.Tensor | None = None,
+                        k_out: torch.Tensor | None = None):
+    """Rotates q (B, S, Hq, D) into q_out and k (B, S, Hk, D) into k_out with
+    one launch, tail columns copied: each output equals rope_rotate_half of its
+    input.  Tables or angles as for rope_rotate_half_qk_.  The outputs are
+    allocated when not given (any strides with D contiguous otherwise).
+    Returns (q_out, k_out)."""
+    B, S, Hq, Hk, D, rot, cp, sp, fp = _qk_args(q, k, cos, sin, freqs)
+    if q_out is None:
+        q_out = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if k_out is None:
+        k_out = torch.empty((B, S, Hk, D), dtype=torch.bfloat16, device=k.device)
+    for t, name, like in ((q_out, "q_out", q), (k_out, "k_out", k)):
+        _need(t, name, torch.bfloat16)
+        if t.shape != like.shape:
+            raise ValueError(f"{name} must have the shape of {name[0]}")
+        _last_contiguous(t, name)
+    sq, sk, soq, sok = q.stride(), k.stride(), q_out.stride(), k_out.stride()
+    key = _sc.want("rope_rotate_half_qk_out", q, k, cos if freqs is None else freqs)
+    _capi.check("dtrot_rope_rotate_half_qk_out", q.data_ptr(), Hq, sq[0], sq[1], sq[2],
+                k.data_ptr(), Hk, sk[0], sk[1], sk[2], B, S, D, cp or None, sp or None,
+                fp or None, rot, q_out.data_ptr(), soq[0], soq[1], soq[2], k_out.data_ptr(),
+                sok[0], sok[1], sok[2], _stream(q))
+    if key:
+        _qk_selfcheck([("rope_rotate_half_qk q", q, q_out),
+                            ("rope_rotate_half_qk k", k, k_out)], cos, sin, freqs)
+    return q_out, k_out
 
 
 def _rows(t: torch.Tensor, name: str):

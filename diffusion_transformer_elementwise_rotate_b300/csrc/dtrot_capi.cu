@@ -307,68 +307,95 @@ DTROT_API dtrot_status dtrot_rope_rotate_half(const uint16_t* x, int64_t B, int6
     return launch_status(launch_rope_rotate_half(p, (cudaStream_t)stream));
 }
 
-DTROT_API dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_t sq_b,
-                                                 int64_t sq_s, int64_t sq_h, uint16_t* k,
-                                                 int64_t Hk, int64_t sk_b, int64_t sk_s,
-                                                 int64_t sk_h, int64_t B, int64_t S, int64_t D,
-                                                 const uint16_t* cos, const uint16_t* sin,
-                                                 const float* freqs, int64_t rot_dim,
-                                                 void* stream) {
+// The q and k views of a fused q+k RoPE call, (B, S, Hq, D) and (B, S, Hk, D)
+// with element strides qst, kst (the D stride 1): strides valid, and for the
+// views written (`written`) rows that do not overlap and no element shared
+// between q and k, whose byte ranges are then disjoint or the two head ranges
+// of one (B, S, Hq + Hk, D) view, in either order (the q and k parts of a
+// fused QKV buffer).  Fills the byte spans rq, rk (empty for no heads).
+static dtrot_status qk_views(const uint16_t* q, int64_t Hq, const int64_t* qst,
+                             const uint16_t* k, int64_t Hk, const int64_t* kst, int64_t B,
+                             int64_t S, int64_t D, bool written, Range* rq, Range* rk) {
+    const int64_t qsz[4] = {B, S, Hq, D}, ksz[4] = {B, S, Hk, D};
+    for (int i = 0; i < 3; ++i) {
+        if (Hq > 0 && (qst[i] < 0 || (qsz[i] > 1 && qst[i] == 0))) return DTROT_ERR_STRIDE;
+        if (Hk > 0 && (kst[i] < 0 || (ksz[i] > 1 && kst[i] == 0))) return DTROT_ERR_STRIDE;
+    }
+    if (written && ((Hq > 0 && !non_self_overlapping(qsz, qst, 4)) ||
+                    (Hk > 0 && !non_self_overlapping(ksz, kst, 4))))
+        return DTROT_ERR_STRIDE;
+    *rq = Range{0, 0};
+    *rk = Range{0, 0};
+    if ((Hq > 0 && !span(q, 2, qsz, qst, 4, rq)) || (Hk > 0 && !span(k, 2, ksz, kst, 4, rk)))
+        return DTROT_ERR_SHAPE;
+    if (written && Hq > 0 && Hk > 0 && overlap(*rq, *rk)) {
+        bool ok = qst[0] == kst[0] && qst[1] == kst[1] && qst[2] == kst[2];
+        if (ok) {
+            const uint16_t* first = q < k ? q : k;
+            const uint16_t* second = q < k ? k : q;
+            const int64_t h_first = q < k ? Hq : Hk;
+            int64_t off;
+            ok = mul_ok(h_first, qst[2], &off) && second == first + off;
+            const int64_t usz[4] = {B, S, Hq + Hk, D};
+            ok = ok && non_self_overlapping(usz, qst, 4);
+        }
+        if (!ok) return DTROT_ERR_ALIAS;
+    }
+    return DTROT_OK;
+}
+
+// A fused q+k RoPE call: q, k read (with their strides), qo, ko written
+// (qo == q and ko == k with the same strides in place).
+static dtrot_status rope_qk_call(const uint16_t* q, int64_t Hq, const int64_t* qst,
+                                 const uint16_t* k, int64_t Hk, const int64_t* kst, int64_t B,
+                                 int64_t S, int64_t D, const uint16_t* cos, const uint16_t* sin,
+                                 const float* freqs, int64_t rot_dim, uint16_t* qo,
+                                 const int64_t* qost, uint16_t* ko, const int64_t* kost,
+                                 bool in_place, void* stream) {
     if (B < 0 || S < 0 || Hq < 0 || Hk < 0 || D < 0) return DTROT_ERR_SHAPE;
     int64_t ntok, rows, n;
     if (!mul_ok(B, S, &ntok) || __builtin_add_overflow(Hq, Hk, &rows) ||
         !mul_ok(ntok, rows, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 16, &n))
         return DTROT_ERR_SHAPE;
     if (n == 0) return DTROT_OK;
-    if ((Hq > 0 && !q) || (Hk > 0 && !k)) return DTROT_ERR_NULL;
+    if ((Hq > 0 && (!q || !qo)) || (Hk > 0 && (!k || !ko))) return DTROT_ERR_NULL;
     if (freqs && (cos || sin)) return DTROT_ERR_VALUE;  // tables or angles, not both
     if (!freqs && (!cos || !sin)) return DTROT_ERR_NULL;
     if (rot_dim <= 0 || rot_dim % 2 || rot_dim > D) return DTROT_ERR_ROTDIM;
     int64_t tab;
     if (!mul_ok(ntok, rot_dim, &tab) || !mul_ok(tab, 4, &tab)) return DTROT_ERR_SHAPE;
     tab /= 4;
-    const int64_t qsz[4] = {B, S, Hq, D}, ksz[4] = {B, S, Hk, D};
-    const int64_t qst[4] = {sq_b, sq_s, sq_h, 1}, kst[4] = {sk_b, sk_s, sk_h, 1};
-    for (int i = 0; i < 3; ++i) {
-        if (Hq > 0 && (qst[i] < 0 || (qsz[i] > 1 && qst[i] == 0))) return DTROT_ERR_STRIDE;
-        if (Hk > 0 && (kst[i] < 0 || (ksz[i] > 1 && kst[i] == 0))) return DTROT_ERR_STRIDE;
-    }
-    if ((Hq > 0 && !non_self_overlapping(qsz, qst, 4)) ||
-        (Hk > 0 && !non_self_overlapping(ksz, kst, 4)))
-        return DTROT_ERR_STRIDE;
-    Range rq{0, 0}, rk{0, 0};
-    if ((Hq > 0 && !span(q, 2, qsz, qst, 4, &rq)) || (Hk > 0 && !span(k, 2, ksz, kst, 4, &rk)))
-        return DTROT_ERR_SHAPE;
-    if (Hq > 0 && Hk > 0 && overlap(rq, rk)) {
-        // allowed when q and k are the two head ranges of one (B, S, Hq + Hk, D)
-        // view (the q and k parts of a fused QKV buffer), in either order
-        bool ok = sq_b == sk_b && sq_s == sk_s && sq_h == sk_h;
-        if (ok) {
-            const uint16_t* first = q < k ? q : k;
-            const uint16_t* second = q < k ? k : q;
-            const int64_t h_first = q < k ? Hq : Hk;
-            int64_t off;
-            ok = mul_ok(h_first, sq_h, &off) && second == first + off;
-            const int64_t usz[4] = {B, S, Hq + Hk, D};
-            ok = ok && non_self_overlapping(usz, qst, 4);
-        }
-        if (!ok) return DTROT_ERR_ALIAS;
-    }
-    // the read-only inputs must not overlap what is written
-    Range rin1, rin2{0, 0};
-    if (freqs) {
-        rin1 = Range{(uintptr_t)freqs, (uintptr_t)freqs + (uintptr_t)tab * 4};
+    Range rq, rk, rqo, rko;
+    dtrot_status st = qk_views(q, Hq, qst, k, Hk, kst, B, S, D, in_place, &rq, &rk);
+    if (st != DTROT_OK) return st;
+    if (in_place) {
+        rqo = rq;
+        rko = rk;
     } else {
-        rin1 = Range{(uintptr_t)cos, (uintptr_t)cos + (uintptr_t)tab * 2};
-        rin2 = Range{(uintptr_t)sin, (uintptr_t)sin + (uintptr_t)tab * 2};
+        st = qk_views(qo, Hq, qost, ko, Hk, kost, B, S, D, true, &rqo, &rko);
+        if (st != DTROT_OK) return st;
     }
-    for (const Range* r : {&rq, &rk})
-        if (r->hi > r->lo && (overlap(*r, rin1) || (rin2.hi > rin2.lo && overlap(*r, rin2))))
-            return DTROT_ERR_ALIAS;
+    // nothing read may overlap what is written (in place, q and k themselves)
+    Range rin[4] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}};
+    if (freqs) {
+        rin[0] = Range{(uintptr_t)freqs, (uintptr_t)freqs + (uintptr_t)tab * 4};
+    } else {
+        rin[0] = Range{(uintptr_t)cos, (uintptr_t)cos + (uintptr_t)tab * 2};
+        rin[1] = Range{(uintptr_t)sin, (uintptr_t)sin + (uintptr_t)tab * 2};
+    }
+    if (!in_place) {
+        rin[2] = rq;
+        rin[3] = rk;
+    }
+    for (const Range* w : {&rqo, &rko})
+        for (const Range& r : rin)
+            if (w->hi > w->lo && r.hi > r.lo && overlap(*w, r)) return DTROT_ERR_ALIAS;
     if (!device_ok()) return DTROT_ERR_DEVICE;
     RopeQKParams p;
     p.q = q;
     p.k = k;
+    p.qo = qo;
+    p.ko = ko;
     p.cos = freqs ? nullptr : cos;
     p.sin = freqs ? nullptr : sin;
     p.freqs = freqs;
@@ -378,13 +405,44 @@ DTROT_API dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_
     p.Hk = Hk;
     p.D = D;
     p.rot = rot_dim;
-    p.sq_b = sq_b;
-    p.sq_s = sq_s;
-    p.sq_h = sq_h;
-    p.sk_b = sk_b;
-    p.sk_s = sk_s;
-    p.sk_h = sk_h;
+    p.sq_b = qst[0];
+    p.sq_s = qst[1];
+    p.sq_h = qst[2];
+    p.sk_b = kst[0];
+    p.sk_s = kst[1];
+    p.sk_h = kst[2];
+    p.sqo_b = qost[0];
+    p.sqo_s = qost[1];
+    p.sqo_h = qost[2];
+    p.sko_b = kost[0];
+    p.sko_s = kost[1];
+    p.sko_h = kost[2];
+    p.copy_tail = in_place ? 0 : 1;
     return launch_status(launch_rope_qk(p, (cudaStream_t)stream));
+}
+
+DTROT_API dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_t sq_b,
+                                                 int64_t sq_s, int64_t sq_h, uint16_t* k,
+                                                 int64_t Hk, int64_t sk_b, int64_t sk_s,
+                                                 int64_t sk_h, int64_t B, int64_t S, int64_t D,
+                                                 const uint16_t* cos, const uint16_t* sin,
+                                                 const float* freqs, int64_t rot_dim,
+                                                 void* stream) {
+    const int64_t qst[4] = {sq_b, sq_s, sq_h, 1}, kst[4] = {sk_b, sk_s, sk_h, 1};
+    return rope_qk_call(q, Hq, qst, k, Hk, kst, B, S, D, cos, sin, freqs, rot_dim, q, qst, k,
+                        kst, true, stream);
+}
+
+DTROT_API dtrot_status dtrot_rope_rotate_half_qk_out(
+    const uint16_t* q, int64_t Hq, int64_t sq_b, int64_t sq_s, int64_t sq_h, const uint16_t* k,
+    int64_t Hk, int64_t sk_b, int64_t sk_s, int64_t sk_h, int64_t B, int64_t S, int64_t D,
+    const uint16_t* cos, const uint16_t* sin, const float* freqs, int64_t rot_dim,
+    uint16_t* q_out, int64_t soq_b, int64_t soq_s, int64_t soq_h, uint16_t* k_out,
+    int64_t sok_b, int64_t sok_s, int64_t sok_h, void* stream) {
+    const int64_t qst[4] = {sq_b, sq_s, sq_h, 1}, kst[4] = {sk_b, sk_s, sk_h, 1};
+    const int64_t qost[4] = {soq_b, soq_s, soq_h, 1}, kost[4] = {sok_b, sok_s, sok_h, 1};
+    return rope_qk_call(q, Hq, qst, k, Hk, kst, B, S, D, cos, sin, freqs, rot_dim, q_out, qost,
+                        k_out, kost, false, stream);
 }
 
 // Strides, spans and overlaps of a GEGLU call's gate, up and out; fills p.

@@ -158,14 +158,19 @@ struct RopeParams {
 };
 
 struct RopeQKParams {
-    uint16_t* q;             // (B, S, Hq, D), strides sq_*, rotated in place
-    uint16_t* k;             // (B, S, Hk, D), strides sk_*, rotated in place
+    const uint16_t* q;       // (B, S, Hq, D), strides sq_*
+    const uint16_t* k;       // (B, S, Hk, D), strides sk_*
+    uint16_t* qo;            // rotated q, strides sqo_* (== q, sq_* in place)
+    uint16_t* ko;            // rotated k, strides sko_* (== k, sk_* in place)
     const uint16_t* cos;     // (B*S, rot) tables, or NULL when freqs is given
     const uint16_t* sin;
     const float* freqs;      // (S, B, 1, rot) angles, or NULL when tables are given
     int64_t B, S, Hq, Hk, D, rot;
     int64_t sq_b, sq_s, sq_h;
     int64_t sk_b, sk_s, sk_h;
+    int64_t sqo_b, sqo_s, sqo_h;
+    int64_t sko_b, sko_s, sko_h;
+    int copy_tail;           // out of place: columns [rot, D) are copied to the outputs
 };
 
 struct GemmGegluArgs {

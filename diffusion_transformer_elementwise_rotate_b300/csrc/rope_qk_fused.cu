@@ -1,6 +1,6 @@
 // Rotate-half RoPE on q and k of one attention layer in a single launch, in
-// place, with the cos/sin rows either read from the (B*S, rot_dim) tables or
-// computed on the fly from the rotary angles.
+// place or into separate outputs, with the cos/sin rows either read from the
+// (B*S, rot_dim) tables or computed on the fly from the rotary angles.
 //
 // ERNIE-Image fusion page (sglang PR #34306 analysis): section 2 gives the
 // per-op bf16 rounding of the rotation, round(round(x1*cos1) + round(-x2*sin1)),
@@ -24,8 +24,12 @@
 //     time (the partner's entry copied when its angle has the same bits),
 //     into its slot of shared memory and then reads its vectors from there;
 //     the same registers serve every q and k head of the token;
-//   - tail columns [rot_dim, D) are not touched: in place they already hold x.
-// Generic path: one thread per (token, head row of q or k, pair index).
+//   - tail columns [rot_dim, D) are not touched in place (they already hold
+//     x); out of place, NT = (D - rot_dim) / VW more items per head row copy
+//     them, so a lane's item is a pair (it < NP) or a tail vector, and NP + NT
+//     items share the warp's 32 lanes.
+// Generic path: one thread per (token, head row of q or k, item), items being
+// the pair indices and, out of place, the tail columns.
 #include "dtrot_internal.cuh"
 
 namespace dtrot {
@@ -79,32 +83,40 @@ __device__ __forceinline__ void qk_rot(uint32_t a, uint32_t b, uint32_t c1, uint
 struct QKArgs {
     RopeQKParams p;
     int NP;   // pair items per head row
+    int NI;   // items per head row: the NP pairs, then the tail items
     int RPW;  // head rows per warp pass
 };
 
-template <int VW, int U, bool ANGLES>
+// TAIL: out of place with tail columns, so some lanes copy instead of rotate.
+template <int VW, int U, bool ANGLES, bool TAIL>
 __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
     using V = typename QKVec<VW>::T;
     __shared__ __align__(16) uint16_t cs[kWarps][2][kMaxRot];  // angle mode: cos, sin row
     pdl_wait();
     const RopeQKParams& p = a.p;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int ri = lane / a.NP;
-    const int it = lane - ri * a.NP;
-    const bool active = ri < a.RPW;  // 32 may not be a multiple of NP
+    const int ri = lane / a.NI;
+    const int it = lane - ri * a.NI;
+    const bool active = ri < a.RPW;  // 32 may not be a multiple of NI
+    const bool pair = !TAIL || it < a.NP;
     const int64_t ntok = p.B * p.S;
     const int64_t warps = (int64_t)gridDim.x * kWarps;
     const int64_t hh = p.rot >> 1;
-    const int64_t j = (int64_t)it * VW;
+    const int64_t j = pair ? (int64_t)it * VW : p.rot + (int64_t)(it - a.NP) * VW;
     const int64_t rows = p.Hq + p.Hk;  // q rows, then k rows
     const int64_t step = (int64_t)U * a.RPW;
     for (int64_t tok = (int64_t)blockIdx.x * kWarps + w; tok < ntok; tok += warps) {
         const int64_t b = tok / p.S;
         const int64_t s = tok - b * p.S;
-        uint16_t* qb = p.q + b * p.sq_b + s * p.sq_s + j;
-        uint16_t* kb = p.k + b * p.sk_b + s * p.sk_s + j;
-        auto row_ptr = [&](int64_t r) {
+        const uint16_t* qb = p.q + b * p.sq_b + s * p.sq_s + j;
+        const uint16_t* kb = p.k + b * p.sk_b + s * p.sk_s + j;
+        uint16_t* qob = p.qo + b * p.sqo_b + s * p.sqo_s + j;
+        uint16_t* kob = p.ko + b * p.sko_b + s * p.sko_s + j;
+        auto in_row = [&](int64_t r) {
             return r < p.Hq ? qb + r * p.sq_h : kb + (r - p.Hq) * p.sk_h;
+        };
+        auto out_row = [&](int64_t r) {
+            return r < p.Hq ? qob + r * p.sqo_h : kob + (r - p.Hq) * p.sko_h;
         };
         // the first batch of head rows is loaded before the cos/sin row is
         // fetched or evaluated, so its memory latency overlaps that work
@@ -114,14 +126,14 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int64_t r = r0 + (int64_t)u * a.RPW;
                 if (active && r < rows) {
-                    const uint16_t* ptr = row_ptr(r);
+                    const uint16_t* ptr = in_row(r);
                     xa[u] = qk_ld<VW>(ptr);
-                    xb[u] = qk_ld<VW>(ptr + hh);
+                    if (pair) xb[u] = qk_ld<VW>(ptr + hh);
                 }
             }
         };
         load_batch(ri);
-        V c1, c2, s1, s2;
+        V c1{}, c2{}, s1{}, s2{};
         if constexpr (ANGLES) {
             // column c of the first half and its partner c + hh: a partner
             // angle with the same bits has the same entry, which is copied
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
                 cs[w][1][c + hh] = sv;
             }
             __syncwarp();
-            if (active) {
+            if (active && pair) {
                 c1 = qk_ld<VW>(&cs[w][0][j]);
                 c2 = qk_ld<VW>(&cs[w][0][j + hh]);
                 s1 = qk_ld<VW>(&cs[w][1][j]);
@@ -151,7 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
             }
             __syncwarp();  // every lane has its row before the next token overwrites it
         } else {
-            if (active) {
+            if (active && pair) {
                 const uint16_t* ct = p.cos + tok * p.rot + j;
                 const uint16_t* st = p.sin + tok * p.rot + j;
                 c1 = qk_ld<VW>(ct);
@@ -166,11 +178,15 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int64_t r = r0 + (int64_t)u * a.RPW;
                 if (r < rows) {
-                    V o1, o2;
-                    qk_rot(xa[u], xb[u], c1, s1, c2, s2, o1, o2);
-                    uint16_t* ptr = row_ptr(r);
-                    qk_st<VW>(ptr, o1);
-                    qk_st<VW>(ptr + hh, o2);
+                    uint16_t* ptr = out_row(r);
+                    if (pair) {
+                        V o1, o2;
+                        qk_rot(xa[u], xb[u], c1, s1, c2, s2, o1, o2);
+                        qk_st<VW>(ptr, o1);
+                        qk_st<VW>(ptr + hh, o2);
+                    } else {
+                        qk_st<VW>(ptr, xa[u]);
+                    }
                 }
             }
             r0 += step;
@@ -180,25 +196,34 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
     }
 }
 
-// Generic path: one thread per (token, head row, pair index i < hh); head rows
-// [0, Hq) are q's, [Hq, Hq + Hk) k's.
+// Generic path: one thread per (token, head row, item); head rows [0, Hq) are
+// q's, [Hq, Hq + Hk) k's; item i < hh is the pair (i, i + hh), item i >= hh
+// (out of place only) copies tail column rot + (i - hh).
 template <bool ANGLES>
 __global__ void __launch_bounds__(256) rope_qk_generic_kernel(RopeQKParams p) {
     pdl_wait();
     const int64_t hh = p.rot >> 1;
     const int64_t rows = p.Hq + p.Hk;
-    const int64_t per_tok = rows * hh;
+    const int64_t items = hh + (p.copy_tail ? p.D - p.rot : 0);
+    const int64_t per_tok = rows * items;
     const int64_t total = p.B * p.S * per_tok;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t tok = g / per_tok;
         const int64_t rem = g - tok * per_tok;
-        const int64_t r = rem / hh;
-        const int64_t i = rem - r * hh;
+        const int64_t r = rem / items;
+        const int64_t i = rem - r * items;
         const int64_t b = tok / p.S;
         const int64_t s = tok - b * p.S;
-        uint16_t* row = r < p.Hq ? p.q + b * p.sq_b + s * p.sq_s + r * p.sq_h
-                                 : p.k + b * p.sk_b + s * p.sk_s + (r - p.Hq) * p.sk_h;
+        const uint16_t* row = r < p.Hq ? p.q + b * p.sq_b + s * p.sq_s + r * p.sq_h
+                                       : p.k + b * p.sk_b + s * p.sk_s + (r - p.Hq) * p.sk_h;
+        uint16_t* orow = r < p.Hq ? p.qo + b * p.sqo_b + s * p.sqo_s + r * p.sqo_h
+                                  : p.ko + b * p.sko_b + s * p.sko_s + (r - p.Hq) * p.sko_h;
+        if (i >= hh) {
+            const int64_t c = p.rot + (i - hh);
+            orow[c] = row[c];
+            continue;
+        }
         uint32_t c1, c2, s1, s2;
         if constexpr (ANGLES) {
             const float* fr = p.freqs + (s * p.B + b) * p.rot;
@@ -214,19 +239,27 @@ __global__ void __launch_bounds__(256) rope_qk_generic_kernel(RopeQKParams p) {
         }
         uint32_t o1, o2;
         qk_rot_word(row[i], row[i + hh], c1, s1, c2, s2, o1, o2);
-        row[i] = (uint16_t)o1;
-        row[i + hh] = (uint16_t)o2;
+        orow[i] = (uint16_t)o1;
+        orow[i + hh] = (uint16_t)o2;
     }
 }
 
 bool aligned(const void* ptr, int bytes) { return ((uintptr_t)ptr % bytes) == 0; }
 
+// Every pointer and stride of the q side (and of the k side) a multiple of vw
+// elements, for a tensor whose head count is n.
+bool vec_ok(int vw, int64_t n, const void* ptr, int64_t sb, int64_t ss, int64_t sh) {
+    return n == 0 || (sb % vw == 0 && ss % vw == 0 && sh % vw == 0 && aligned(ptr, 2 * vw));
+}
+
 int pick_qk_vw(const RopeQKParams& p) {
     const int64_t hh = p.rot / 2;
     for (int vw = 8; vw >= 2; vw >>= 1) {
-        if (hh % vw) continue;
-        if ((p.Hq > 0 && (p.sq_b % vw || p.sq_s % vw || p.sq_h % vw || !aligned(p.q, 2 * vw))) ||
-            (p.Hk > 0 && (p.sk_b % vw || p.sk_s % vw || p.sk_h % vw || !aligned(p.k, 2 * vw))))
+        if (hh % vw || (p.copy_tail && p.D % vw)) continue;
+        if (!vec_ok(vw, p.Hq, p.q, p.sq_b, p.sq_s, p.sq_h) ||
+            !vec_ok(vw, p.Hq, p.qo, p.sqo_b, p.sqo_s, p.sqo_h) ||
+            !vec_ok(vw, p.Hk, p.k, p.sk_b, p.sk_s, p.sk_h) ||
+            !vec_ok(vw, p.Hk, p.ko, p.sko_b, p.sko_s, p.sko_h))
             continue;
         if (!p.freqs && (!aligned(p.cos, 2 * vw) || !aligned(p.sin, 2 * vw))) continue;
         return vw;
@@ -234,31 +267,42 @@ int pick_qk_vw(const RopeQKParams& p) {
     return 1;
 }
 
-template <int VW, bool ANGLES>
+template <int VW, bool ANGLES, bool TAIL>
 cudaError_t launch_qk_fast(const QKArgs& a, cudaStream_t st) {
     const int64_t ntok = a.p.B * a.p.S;
     int64_t blocks = (ntok + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    return launch_pdl(rope_qk_kernel<VW, 4, ANGLES>, dim3((unsigned)blocks), dim3(kWarps * 32), 0,
-                      st, a);
+    return launch_pdl(rope_qk_kernel<VW, 4, ANGLES, TAIL>, dim3((unsigned)blocks),
+                      dim3(kWarps * 32), 0, st, a);
+}
+
+template <int VW, bool ANGLES>
+cudaError_t launch_qk_fast(const QKArgs& a, cudaStream_t st) {
+    return a.NI > a.NP ? launch_qk_fast<VW, ANGLES, true>(a, st)
+                       : launch_qk_fast<VW, ANGLES, false>(a, st);
 }
 
 template <bool ANGLES>
 cudaError_t launch_qk(const RopeQKParams& p, cudaStream_t st) {
     const int vw = pick_qk_vw(p);
     const int64_t hh = p.rot / 2;
-    if (vw >= 2 && hh / vw <= 32 && (!ANGLES || p.rot <= kMaxRot)) {
+    if (vw >= 2 && (!ANGLES || p.rot <= kMaxRot)) {
         QKArgs a;
         a.p = p;
         a.NP = (int)(hh / vw);
-        a.RPW = 32 / a.NP;
-        switch (vw) {
-            case 8: return launch_qk_fast<8, ANGLES>(a, st);
-            case 4: return launch_qk_fast<4, ANGLES>(a, st);
-            default: return launch_qk_fast<2, ANGLES>(a, st);
+        const int64_t ni = hh / vw + (p.copy_tail ? (p.D - p.rot) / vw : 0);
+        if (ni <= 32) {
+            a.NI = (int)ni;
+            a.RPW = 32 / a.NI;
+            switch (vw) {
+                case 8: return launch_qk_fast<8, ANGLES>(a, st);
+                case 4: return launch_qk_fast<4, ANGLES>(a, st);
+                default: return launch_qk_fast<2, ANGLES>(a, st);
+            }
         }
     }
-    const int64_t total = p.B * p.S * (p.Hq + p.Hk) * hh;
+    const int64_t total =
+        p.B * p.S * (p.Hq + p.Hk) * (hh + (p.copy_tail ? p.D - p.rot : 0));
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;

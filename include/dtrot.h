@@ -147,6 +147,34 @@ dtrot_status dtrot_rope_rotate_half_qk(uint16_t* q, int64_t Hq, int64_t sq_b, in
                                        const float* freqs, int64_t rot_dim, void* stream);
 
 /*
+ * Rotate-half RoPE on q and k in one launch, into separate outputs.
+ *                                                        [P4] sections 1-2
+ *
+ * The out-of-place form of dtrot_rope_rotate_half_qk: q_out receives the
+ * rotation of q and k_out that of k, tail columns [rot_dim, D) copied, so
+ * each output equals what dtrot_rope_rotate_half writes for its input, bit
+ * for bit.  One launch for both instead of one per tensor saves a kernel
+ * boundary per layer.
+ *   q, k        bf16, (B, S, Hq, D) and (B, S, Hk, D), element strides
+ *               (sq_*), (sk_*), D contiguous, read only.  q may be NULL when
+ *               Hq == 0, k when Hk == 0.  They may overlap each other.
+ *   cos, sin, freqs, rot_dim   as for dtrot_rope_rotate_half_qk.
+ *   q_out       bf16, (B, S, Hq, D), strides (soq_*), written; k_out
+ *               likewise (sok_*).  Each must have non-overlapping rows
+ *               (DTROT_ERR_STRIDE); the two must not share elements (their
+ *               byte ranges disjoint, or the two head ranges of one
+ *               (B, S, Hq + Hk, D) view); neither may overlap q, k, the
+ *               tables or the angles (DTROT_ERR_ALIAS).  For in place, use
+ *               dtrot_rope_rotate_half_qk.
+ */
+dtrot_status dtrot_rope_rotate_half_qk_out(
+    const uint16_t* q, int64_t Hq, int64_t sq_b, int64_t sq_s, int64_t sq_h, const uint16_t* k,
+    int64_t Hk, int64_t sk_b, int64_t sk_s, int64_t sk_h, int64_t B, int64_t S, int64_t D,
+    const uint16_t* cos, const uint16_t* sin, const float* freqs, int64_t rot_dim,
+    uint16_t* q_out, int64_t soq_b, int64_t soq_s, int64_t soq_h, uint16_t* k_out,
+    int64_t sok_b, int64_t sok_s, int64_t sok_h, void* stream);
+
+/*
  * Bytes of device workspace dtrot_gelu_and_mul needs (its activation table:
  * 65536 bf16 entries, 131072 bytes).  Constant for a given library version.
  */

@@ -42,7 +42,8 @@ def declared_functions():
 def test_header_declares_the_four_ops():
     names = declared_functions()
     for op in ("dtrot_rope_cos_sin_precompute", "dtrot_rope_rotate_half",
-               "dtrot_rope_rotate_half_qk", "dtrot_gelu_and_mul",
+               "dtrot_rope_rotate_half_qk", "dtrot_rope_rotate_half_qk_out",
+               "dtrot_gelu_and_mul",
                "dtrot_gelu_and_mul_workspace_bytes", "dtrot_gelu_table_build",
                "dtrot_gelu_and_mul_with_table", "dtrot_gemm_gelu_and_mul",
                "dtrot_gemm_gelu_and_mul_workspace_bytes", "dtrot_gemm_gelu_and_mul_error",
@@ -143,6 +144,50 @@ def test_rope_qk_valid_layouts_reach_the_device_check(lib):
     assert rope_qk(cos=0, sin=0, freqs=Q) == _capi.ERR_DEVICE          # angles
 
 
+def rope_qk_out(**kw):
+    # q heads [0, 2) and k heads [2, 4) of one (1, 4, 6, 8) QKV buffer at P,
+    # rotated into the two head ranges of one (1, 4, 4, 8) buffer at W
+    a = dict(q=P, Hq=2, sq_b=192, sq_s=48, sq_h=8, k=P + 2 * 16, Hk=2, sk_b=192, sk_s=48, sk_h=8,
+             B=1, S=4, D=8, cos=Q, sin=R, freqs=0, rot=8,
+             qo=W, soq_b=128, soq_s=32, soq_h=8, ko=W + 2 * 16, sok_b=128, sok_s=32, sok_h=8)
+    a.update(kw)
+    return _capi.call("dtrot_rope_rotate_half_qk_out", a["q"] or None, a["Hq"], a["sq_b"],
+                      a["sq_s"], a["sq_h"], a["k"] or None, a["Hk"], a["sk_b"], a["sk_s"],
+                      a["sk_h"], a["B"], a["S"], a["D"], a["cos"] or None, a["sin"] or None,
+                      a["freqs"] or None, a["rot"], a["qo"] or None, a["soq_b"], a["soq_s"],
+                      a["soq_h"], a["ko"] or None, a["sok_b"], a["sok_s"], a["sok_h"], None)
+
+
+def test_rope_qk_out_validation(lib):
+    assert rope_qk_out(S=0, q=0, k=0, cos=0, sin=0, qo=0, ko=0) == _capi.OK
+    assert rope_qk_out(Hq=0, Hk=0) == _capi.OK
+    assert rope_qk_out(q=0) == _capi.ERR_NULL
+    assert rope_qk_out(ko=0) == _capi.ERR_NULL
+    assert rope_qk_out(sin=0) == _capi.ERR_NULL
+    assert rope_qk_out(freqs=WS) == _capi.ERR_VALUE                    # tables and angles
+    assert rope_qk_out(rot=10) == _capi.ERR_ROTDIM
+    assert rope_qk_out(Hq=-2) == _capi.ERR_SHAPE
+    assert rope_qk_out(sq_s=0) == _capi.ERR_STRIDE                     # input stride 0
+    assert rope_qk_out(soq_h=0) == _capi.ERR_STRIDE
+    assert rope_qk_out(sok_h=4) == _capi.ERR_STRIDE                    # k_out rows overlap
+    assert rope_qk_out(ko=W + 2 * 8) == _capi.ERR_ALIAS                # k_out inside q_out
+    assert rope_qk_out(ko=W + 2 * 16, sok_s=64) == _capi.ERR_ALIAS     # interleaved, other strides
+    assert rope_qk_out(qo=P) == _capi.ERR_ALIAS                        # output over q
+    assert rope_qk_out(ko=P + 2 * 32, sok_b=192, sok_s=48) == _capi.ERR_ALIAS  # over q's span
+    assert rope_qk_out(cos=W + 2 * 40) == _capi.ERR_ALIAS              # tables under k_out
+    assert rope_qk_out(cos=0, sin=0, freqs=W) == _capi.ERR_ALIAS       # angles under q_out
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host without a GPU only")
+@no_device
+def test_rope_qk_out_valid_layouts_reach_the_device_check(lib):
+    assert rope_qk_out() == _capi.ERR_DEVICE                            # fused in, fused out
+    assert rope_qk_out(k=P) == _capi.ERR_DEVICE                         # inputs may overlap
+    assert rope_qk_out(Hk=0, k=0, ko=0) == _capi.ERR_DEVICE             # q alone
+    assert rope_qk_out(ko=R + 4096, sok_b=64, sok_s=16) == _capi.ERR_DEVICE  # separate outputs
+    assert rope_qk_out(cos=0, sin=0, freqs=Q) == _capi.ERR_DEVICE       # angles
+
+
 def gemm(**kw):
     a = dict(x=P, T=4, C=64, w=Q, F=16, out=R, so=16, gu=0, sgu=32, ws=WS, wsb=17408)
     a.update(kw)
@@ -203,6 +248,7 @@ def test_zero_sized_calls_are_noops(lib):
     assert geglu(T=0, gate=0, up=0, out=0) == _capi.OK
     assert rms(C=0, x=0, res=0, w=0, out=0) == _capi.OK
     assert tables(S=0, f=0, c=0, s=0) == _capi.OK
+    assert rope_qk_out(B=0, q=0, k=0, cos=0, sin=0, qo=0, ko=0) == _capi.OK
 
 
 def test_null_pointers(lib):

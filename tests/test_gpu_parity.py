@@ -219,8 +219,11 @@ def test_rope_empty():
 
 # ---------------------------------------------------------------- q and k in one launch
 
-def _qk_check(B, S, Hq, Hk, D, rot, freqs, seed, mode, layout="qkv", offset=0):
-    """RoPE on q and k in place, in one launch, against the oracle on each."""
+def _qk_check(B, S, Hq, Hk, D, rot, freqs, seed, mode, layout="qkv", offset=0, out=None):
+    """RoPE on q and k in one launch against the oracle on each: in place
+    (out=None), or out of place into separate outputs with padded head rows
+    (out="separate") or into the q and k head ranges of one output buffer
+    (out="fused"); out of place, the inputs and the padding stay unchanged."""
     Hv = Hq if layout == "qkv" else 0
     if layout == "qkv":
         buf = W.normal_bf16((B, S, Hq + Hk + Hv, D), seed, 0)
@@ -240,12 +243,33 @@ def _qk_check(B, S, Hq, Hk, D, rot, freqs, seed, mode, layout="qkv", offset=0):
         q0, k0 = bits(qh), bits(kh)
     ec, es = oracle.rope_cos_sin(freqs.numpy())
     if mode == "angles":
-        dt.rope_rotate_half_qk_(q, k, freqs=to_dev(freqs))
+        kw = {"freqs": to_dev(freqs)}
     else:
-        dt.rope_rotate_half_qk_(q, k, cos=to_dev(from_u16(ec)), sin=to_dev(from_u16(es)))
+        kw = {"cos": to_dev(from_u16(ec)), "sin": to_dev(from_u16(es))}
+    if out is None:
+        dt.rope_rotate_half_qk_(q, k, **kw)
+        rq, rk = q, k
+    else:
+        pad = 0 if out == "fused" else 16
+        nan = float("nan")
+        if out == "fused":
+            obuf = torch.full((B, S, Hq + Hk, D), nan, dtype=torch.bfloat16, device=DEV)
+            qo, ko = obuf[:, :, :Hq], obuf[:, :, Hq:]
+        else:
+            qpad = torch.full((B, S, Hq, D + pad), nan, dtype=torch.bfloat16, device=DEV)
+            kpad = torch.full((B, S, Hk, D + pad), nan, dtype=torch.bfloat16, device=DEV)
+            qo, ko = qpad[..., :D], kpad[..., :D]
+        rq, rk = dt.rope_rotate_half_qk(q, k, q_out=qo, k_out=ko, **kw)
+        assert rq is qo and rk is ko
+        torch.cuda.synchronize()
+        assert_bitexact(bits(q), q0, "q input unchanged")
+        assert_bitexact(bits(k), k0, "k input unchanged")
+        if pad:
+            for t in (qpad, kpad):
+                assert (bits(t)[..., D:] == 0x7FC0).all(), "padding written"
     torch.cuda.synchronize()
-    assert_bitexact(bits(q), oracle.rope_rotate_half(q0, ec, es), f"q {mode}")
-    assert_bitexact(bits(k), oracle.rope_rotate_half(k0, ec, es), f"k {mode}")
+    assert_bitexact(bits(rq), oracle.rope_rotate_half(q0, ec, es), f"q {mode} {out}")
+    assert_bitexact(bits(rk), oracle.rope_rotate_half(k0, ec, es), f"k {mode} {out}")
     if v is not None:
         assert_bitexact(bits(v), v0, "v untouched")
 
@@ -297,6 +321,67 @@ def test_rope_qk_angles_second_half_reused_only_for_identical_bits():
     nan_b = np.array([0xFFC00002], dtype=np.uint32).view(np.float32)[0]
     f[4, 0, 0, 1], f[4, 0, 0, R // 2 + 1] = float(nan_a), float(nan_b)
     _qk_check(B, S, 3, 2, R, R, f.contiguous(), 77, "angles")
+
+
+@pytest.mark.parametrize("out", ["separate", "fused"])
+@pytest.mark.parametrize("mode", ["tables", "angles"])
+@pytest.mark.parametrize("name", ["tiny", "image", "cfg"])
+def test_rope_qk_out_of_place_configs(name, mode, out):
+    # image: rot 96 of D 128, so out of place the tail columns are copied
+    wl = W.WORKLOADS[name]
+    _qk_check(wl.B, wl.S, wl.H, wl.H, wl.D, wl.rot, W.freqs_for(wl), wl.seed + 60, mode,
+              out=out)
+
+
+@pytest.mark.parametrize("mode", ["tables", "angles"])
+@pytest.mark.parametrize("D,rot", SWEEP)
+def test_rope_qk_out_of_place_sweep_odd_S_gqa(D, rot, mode):
+    B, S = 1, 4097
+    _qk_check(B, S, 6, 2, D, rot, W.freqs_1d(S, B, rot), 190 + D + rot, mode, out="separate")
+
+
+@pytest.mark.parametrize("mode", ["tables", "angles"])
+def test_rope_qk_out_of_place_misaligned_wide_and_long_tails(mode):
+    _qk_check(2, 37, 3, 5, 128, 96, W.freqs_1d(37, 2, 96), 17, mode, layout="separate",
+              out="separate")
+    _qk_check(2, 37, 3, 3, 128, 96, W.freqs_1d(37, 2, 96), 18, mode, offset=1,
+              out="separate")                                                   # scalar path
+    _qk_check(1, 19, 2, 2, 640, 576, W.freqs_1d(19, 1, 576), 19, mode, out="fused")  # rot > 256
+    # 4 pair and 56 tail vectors per head row: more items than lanes, generic path
+    _qk_check(1, 45, 3, 1, 512, 64, W.freqs_1d(45, 1, 64), 20, mode, out="separate")
+    # 4 pair and 4 tail vectors: every lane busy, 4 rows per warp pass
+    _qk_check(1, 45, 5, 3, 96, 64, W.freqs_1d(45, 1, 64), 21, mode, out="fused")
+
+
+def test_rope_qk_out_of_place_equals_rope_rotate_half():
+    # the single launch gives what two rope_rotate_half calls give, bit for bit
+    wl = W.WORKLOADS["image"]
+    freqs = to_dev(W.freqs_for(wl))
+    q, k = to_dev(W.rope_inputs(wl, "q")), to_dev(W.rope_inputs(wl, "k"))
+    c, s = dt.rope_cos_sin_precompute(freqs)
+    qo, ko = dt.rope_rotate_half_qk(q, k, cos=c, sin=s)
+    assert np.array_equal(bits(qo), bits(dt.rope_rotate_half(q, c, s)))
+    assert np.array_equal(bits(ko), bits(dt.rope_rotate_half(k, c, s)))
+
+
+@pytest.mark.parametrize("mode", ["angles", "tables"])
+def test_rope_qk_out_of_place_video_full_size_sampled_tokens(mode):
+    wl = W.WORKLOADS["video"]
+    q, k = W.rope_inputs(wl, "q"), W.rope_inputs(wl, "k")
+    freqs = W.freqs_for(wl)
+    dq, dk = to_dev(q), to_dev(k)
+    if mode == "angles":
+        qo, ko = dt.rope_rotate_half_qk(dq, dk, freqs=to_dev(freqs))
+    else:
+        c, s = dt.rope_cos_sin_precompute(to_dev(freqs))
+        qo, ko = dt.rope_rotate_half_qk(dq, dk, cos=c, sin=s)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    toks = np.unique(np.concatenate([[0, wl.S - 1], rng.choice(wl.S, 512, replace=False)]))
+    ec, es = oracle.rope_cos_sin(freqs.numpy()[toks])
+    assert_bitexact(bits(qo)[:, toks], oracle.rope_rotate_half(bits(q)[:, toks], ec, es), "q")
+    assert_bitexact(bits(ko)[:, toks], oracle.rope_rotate_half(bits(k)[:, toks], ec, es), "k")
+    assert_bitexact(bits(dq)[:, toks], bits(q)[:, toks], "q input unchanged")
 
 
 @pytest.mark.parametrize("mode", ["angles", "tables"])

@@ -107,6 +107,8 @@ def test_every_op_passes_the_check_on_the_gpu():
             dt.rope_rotate_half(q, c, s, out=q)                 # in place
             dt.rope_rotate_half_qk_(q, k, cos=c, sin=s)
             dt.rope_rotate_half_qk_(q, k, freqs=freqs)
+            dt.rope_rotate_half_qk(q, k, cos=c, sin=s)          # out of place
+            dt.rope_rotate_half_qk(q, k, freqs=freqs)
             dt.gelu_and_mul_fused(W.geglu_inputs(wl).cuda())
             x, r, w = (t.cuda() for t in W.rmsnorm_inputs(wl))
             dt.rmsnorm_residual(x, r, w, 1e-6)
@@ -118,7 +120,8 @@ def test_every_op_passes_the_check_on_the_gpu():
             dt.gemm_gelu_and_mul(xm, wm.to(torch.bfloat16))
         ops = {k[0] for k in sc.checked()}
         assert ops == {"rope_cos_sin_precompute", "rope_rotate_half", "rope_rotate_half_qk",
-                       "gelu_and_mul", "rmsnorm_residual", "gemm_gelu_and_mul"}
+                       "rope_rotate_half_qk_out", "gelu_and_mul", "rmsnorm_residual",
+                       "gemm_gelu_and_mul"}
     finally:
         sc.disable()
         sc.reset()
