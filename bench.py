@@ -37,23 +37,41 @@ PKG = "diffusion_transformer_elementwise_rotate_b300"
 METRIC = "fused RoPE/GEGLU/RMSNorm HBM GB/s and % of B300 peak; Mtokens/s per layer"
 FALLBACK_HBM_GBS = 6400.0
 NOMINAL_HBM_GBS = 7700.0
-OPS = ["rope_cos_sin_precompute", "rope_rotate_half_q", "rope_rotate_half_k", "gelu_and_mul",
-       "rmsnorm_residual_attn", "rmsnorm_residual_ffn"]
+# The RoPE of the step on q and on k: both in one launch (rope_rotate_half_qk,
+# out of place, the default) or one rope_rotate_half call per tensor.  Both
+# write the same bits; the single launch saves a kernel boundary and one read
+# of the tables.
+ROPE_FORMS = {"qk": ["rope_rotate_half_qk"],
+              "separate": ["rope_rotate_half_q", "rope_rotate_half_k"]}
 DOMINANT = "gelu_and_mul"
 MIN_DOM_LAUNCHES = 20  # the dominant kernel's roofline is the median of at least this many calls
 PER_WORKLOAD = ("image", "cfg")  # other layer shapes reported beside the headline layer
-# kernels per step: tables 1, RoPE 2, GEGLU 2 (activation table + streaming), RMSNorm 2
-LAUNCHES_PER_STEP = 7
 
 
-def config_for(wl, per_step, parallelism):
+def step_ops(rope="qk"):
+    """The step's calls in order (each a range between two timing events)."""
+    return (["rope_cos_sin_precompute"] + ROPE_FORMS[rope]
+            + ["gelu_and_mul", "rmsnorm_residual_attn", "rmsnorm_residual_ffn"])
+
+
+def launches_per_step(rope="qk"):
+    """Kernels per step: one per call, and two for GEGLU (activation table and
+    streaming kernel)."""
+    return len(step_ops(rope)) + 1
+
+
+
+
+def config_for(wl, per_step, parallelism, rope="qk"):
     """The `config` of both arms' lines: the workload they measure."""
     return {
         "workload": (f"{wl.name} DiT layer: q,k ({wl.B},{wl.S},{wl.H},{wl.D}) rot {wl.rot} "
                      f"split {'/'.join(map(str, wl.split))}; GEGLU ({wl.T_ff}, 2x{wl.F}); "
                      f"RMSNorm+residual ({wl.T_norm}, {wl.C}) x2; cos/sin tables "
                      f"({wl.tokens}, {wl.rot})"),
-        "step": "tables + RoPE q + RoPE k + GEGLU + 2x RMSNorm+residual",
+        "step": ("tables + RoPE q and k (one launch, out of place) + GEGLU + 2x RMSNorm+residual"
+                 if rope == "qk" else
+                 "tables + RoPE q + RoPE k + GEGLU + 2x RMSNorm+residual"),
         "bytes_per_step": per_step,
         "l2": "inputs larger than L2 (126 MB) for every kernel; no flush",
         "parallelism": parallelism,
@@ -69,6 +87,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", default="qk", choices=sorted(ROPE_FORMS),
+                    help="RoPE on q and k in one launch (qk) or one call per tensor (separate)")
     return ap.parse_args()
 
 
@@ -115,16 +135,28 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(wl, W):
+def step_bytes(wl, W, rope="qk"):
+    """Algorithmic bytes of each call of the step."""
     b = W.algorithmic_bytes(wl)
-    return {
+    per_op = {
         "rope_cos_sin_precompute": b["rope_cos_sin_precompute"],
+        "rope_rotate_half_qk": b["rope_rotate_half_qk"],
         "rope_rotate_half_q": b["rope_rotate_half"],
         "rope_rotate_half_k": b["rope_rotate_half"],
         "gelu_and_mul": b["gelu_and_mul"],
         "rmsnorm_residual_attn": b["rmsnorm_residual"],
         "rmsnorm_residual_ffn": b["rmsnorm_residual"],
     }
+    return {op: per_op[op] for op in step_ops(rope)}
+
+
+def sampled_bytes(bts, wl, tok, rows_ff, rows_n):
+    """The algorithmic bytes of the step on a sample of the layer: the first
+    `tok` positions for the tables and RoPE, `rows_ff` GEGLU rows and `rows_n`
+    rows of each RMSNorm (every op's bytes are proportional to its rows)."""
+    frac = {"gelu_and_mul": rows_ff / wl.T_ff, "rmsnorm_residual_attn": rows_n / wl.T_norm,
+            "rmsnorm_residual_ffn": rows_n / wl.T_norm}
+    return sum(v * frac.get(op, tok / wl.S) for op, v in bts.items())
 
 
 def code_text(src: str) -> str:
@@ -235,8 +267,10 @@ class ClockSampler:
 class Layer:
     """One layer's tensors on the device plus pinned host copies."""
 
-    def __init__(self, wl, W, dev, keep_host=True):
+    def __init__(self, wl, W, dev, keep_host=True, rope="qk"):
         self.wl = wl
+        self.rope = rope
+        self.ops = step_ops(rope)
         pin = torch.cuda.is_available() and keep_host
         self.h_in = {
             "freqs": W.freqs_for(wl).pin_memory() if pin else W.freqs_for(wl),
@@ -266,37 +300,46 @@ class Layer:
         return {k: torch.empty_like(v) for k, v in self.d.items()}
 
     def step(self, dt, ev=None, d=None, geglu_kernel_ev=None):
-        """One layer step.  ev: 7 events (or None) for the boundaries around the
-        6 ops.  geglu_kernel_ev: an event to record between GEGLU's two
-        launches; the call is then made as its two C-ABI halves (build the
-        activation table into the same per-stream workspace, then the streaming
-        kernel on it), the very kernels dtrot_gelu_and_mul launches."""
+        """One layer step.  ev: len(self.ops) + 1 events (or None) for the
+        boundaries around the calls.  geglu_kernel_ev: an event to record
+        between GEGLU's two launches; the call is then made as its two C-ABI
+        halves (build the activation table into the same per-stream workspace,
+        then the streaming kernel on it), the very kernels dtrot_gelu_and_mul
+        launches."""
         d, F = (self.d if d is None else d), self.wl.F
 
-        def mark(i):
+        def geglu():
+            gate, up = d["gate_up"][:, :F], d["gate_up"][:, F:]
+            if geglu_kernel_ev is None:
+                dt.gelu_and_mul(gate, up, out=d["ff_out"])
+            else:
+                st = torch.cuda.current_stream(gate.device).cuda_stream
+                ws = dt.gelu_table_build(dt.gelu_workspace(gate.device, st))
+                geglu_kernel_ev.record()
+                dt.gelu_and_mul(gate, up, out=d["ff_out"], table=ws)
+
+        calls = {
+            "rope_cos_sin_precompute":
+                lambda: dt.rope_cos_sin_precompute(d["freqs"], d["cos"], d["sin"]),
+            "rope_rotate_half_qk":
+                lambda: dt.rope_rotate_half_qk(d["q"], d["k"], cos=d["cos"], sin=d["sin"],
+                                               q_out=d["q_out"], k_out=d["k_out"]),
+            "rope_rotate_half_q":
+                lambda: dt.rope_rotate_half(d["q"], d["cos"], d["sin"], out=d["q_out"]),
+            "rope_rotate_half_k":
+                lambda: dt.rope_rotate_half(d["k"], d["cos"], d["sin"], out=d["k_out"]),
+            "gelu_and_mul": geglu,
+            "rmsnorm_residual_attn":
+                lambda: dt.rmsnorm_residual(d["x1"], d["r1"], d["w"], 1e-6, out=d["y1"]),
+            "rmsnorm_residual_ffn":
+                lambda: dt.rmsnorm_residual(d["x2"], d["r2"], d["w"], 1e-6, out=d["y2"]),
+        }
+        for i, op in enumerate(self.ops):
             if ev is not None and ev[i] is not None:
                 ev[i].record()
-
-        mark(0)
-        dt.rope_cos_sin_precompute(d["freqs"], d["cos"], d["sin"])
-        mark(1)
-        dt.rope_rotate_half(d["q"], d["cos"], d["sin"], out=d["q_out"])
-        mark(2)
-        dt.rope_rotate_half(d["k"], d["cos"], d["sin"], out=d["k_out"])
-        mark(3)
-        gate, up = d["gate_up"][:, :F], d["gate_up"][:, F:]
-        if geglu_kernel_ev is None:
-            dt.gelu_and_mul(gate, up, out=d["ff_out"])
-        else:
-            st = torch.cuda.current_stream(gate.device).cuda_stream
-            ws = dt.gelu_table_build(dt.gelu_workspace(gate.device, st))
-            geglu_kernel_ev.record()
-            dt.gelu_and_mul(gate, up, out=d["ff_out"], table=ws)
-        mark(4)
-        dt.rmsnorm_residual(d["x1"], d["r1"], d["w"], 1e-6, out=d["y1"])
-        mark(5)
-        dt.rmsnorm_residual(d["x2"], d["r2"], d["w"], 1e-6, out=d["y2"])
-        mark(6)
+            calls[op]()
+        if ev is not None and ev[len(self.ops)] is not None:
+            ev[len(self.ops)].record()
 
     def h2d(self, d=None):
         d = self.d if d is None else d
@@ -334,21 +377,23 @@ def step_graph(dt, layer, steps, evs=None, kevs=None):
     return g
 
 
-def timing_events(n, which=range(7)):
-    """n sets of 7 external timing events (None where not in `which`)."""
+def timing_events(n, nops, which=None):
+    """n sets of nops + 1 external timing events, one per boundary between the
+    step's calls (None where not in `which`; all when `which` is None)."""
+    which = range(nops + 1) if which is None else which
     return [[torch.cuda.Event(enable_timing=True, external=True) if j in which else None
-             for j in range(7)] for _ in range(n)]
+             for j in range(nops + 1)] for _ in range(n)]
 
 
 def breakdown(dt, layer, steps):
     """Per-op device time (ms, mean over `steps`) from a pass with CUDA events
     between all kernels of the step (a graph of `steps` steps, replayed once)."""
-    evs = timing_events(steps)
+    evs = timing_events(steps, len(layer.ops))
     g = step_graph(dt, layer, steps, evs)
     g.replay()
     torch.cuda.synchronize()
     res = {op: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
-           for j, op in enumerate(OPS)}
+           for j, op in enumerate(layer.ops)}
     del g
     return res
 
@@ -371,7 +416,7 @@ def timed_steps(dt, layer, steps, warm):
     return ms
 
 
-def other_workloads(dt, W, dev, steps, peak):
+def other_workloads(dt, W, dev, steps, peak, rope="qk"):
     """The image and CFG layers: the same step on their shapes, timed like the
     headline layer (a pass of plain steps, then a pass with events between the
     kernels for the per-op figures), each on its own tensors.  Their steps move
@@ -380,25 +425,25 @@ def other_workloads(dt, W, dev, steps, peak):
     res = {}
     for name in PER_WORKLOAD:
         wl = W.WORKLOADS[name]
-        layer = Layer(wl, W, dev, keep_host=False)
-        bts = step_bytes(wl, W)
+        layer = Layer(wl, W, dev, keep_host=False, rope=rope)
+        bts = step_bytes(wl, W, rope)
         per_step = sum(bts.values())
         ms = timed_steps(dt, layer, steps, 3) / steps
         km = breakdown(dt, layer, steps)
         tokens = wl.B * wl.S
         res[name] = {
-            "workload": config_for(wl, per_step, "replicas x1")["workload"],
+            "workload": config_for(wl, per_step, "replicas x1", rope)["workload"],
             "steps": steps,
             "ms_per_step": round(ms, 5),
             "gbs": round(per_step / (ms / 1e3) / 1e9, 1),
             "frac_of_hbm_peak": round(per_step / (ms / 1e3) / 1e9 / peak, 4),
             "mtokens_per_s_per_layer": round(
-                tokens / (sum(km[o] for o in OPS[1:]) / 1e3) / 1e6, 3),
+                tokens / (sum(km[o] for o in layer.ops[1:]) / 1e3) / 1e6, 3),
             "mtokens_per_s_per_step": round(tokens / (ms / 1e3) / 1e6, 3),
             "kernels": {op: {"ms": round(km[op], 5), "bytes": bts[op],
                              "gbs": round(bts[op] / (km[op] / 1e3) / 1e9, 1),
                              "frac_of_hbm_peak": round(bts[op] / (km[op] / 1e3) / 1e9 / peak, 4)}
-                        for op in OPS},
+                        for op in layer.ops},
         }
         del layer
         torch.cuda.empty_cache()
@@ -477,9 +522,54 @@ def fused_rope_qk(dt, layer, wl, reps):
                                           "gbs": round((moved + extra) / (ms / 1e3) / 1e9, 1),
                                           "launches": 1, "reps": reps}
     del q2, k2
-    res["note"] = ("rope_qk: in place, one launch for q and k; 'angles' also replaces the "
-                   "rope_cos_sin_precompute launch of the step.  gemm_gelu_and_mul: the MLP's "
-                   "gate_up projection with GEGLU in its epilogue, gate_up never stored")
+    res["note"] = ("rope_qk_inplace: in place, one launch for q and k; 'angles' also replaces "
+                   "the rope_cos_sin_precompute launch of the step.  rope_qk_out_of_place and "
+                   "rope_two_calls: the step's RoPE in its two forms (--rope qk, the default, "
+                   "and --rope separate).  gemm_gelu_and_mul: the MLP's gate_up projection "
+                   "with GEGLU in its epilogue, gate_up never stored")
+    return res
+
+
+def rope_forms(dt, layer, wl, reps):
+    """The step's RoPE in its two forms, out of place on the layer's q and k
+    with its tables, each timed over `reps` repetitions between two events,
+    alternating in three rounds: one rope_rotate_half_qk launch for both
+    tensors, and two rope_rotate_half calls (one per tensor).  Bytes: q and k
+    read and written once, plus the tables once per launch."""
+    d = layer.d
+    tok = wl.B * wl.S
+    qk_bytes = 8 * tok * wl.H * wl.D
+    forms = {
+        "rope_qk_out_of_place": (
+            lambda: dt.rope_rotate_half_qk(d["q"], d["k"], cos=d["cos"], sin=d["sin"],
+                                           q_out=d["q_out"], k_out=d["k_out"]),
+            qk_bytes + 4 * tok * wl.rot, 1),
+        "rope_two_calls": (
+            lambda: (dt.rope_rotate_half(d["q"], d["cos"], d["sin"], out=d["q_out"]),
+                     dt.rope_rotate_half(d["k"], d["cos"], d["sin"], out=d["k_out"])),
+            qk_bytes + 2 * 4 * tok * wl.rot, 2),
+    }
+    times = {name: [] for name in forms}
+    n = max(1, reps // 3)
+    for _ in range(3):
+        for name, (fn, _, _) in forms.items():
+            for _ in range(3):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times[name].append(e0.elapsed_time(e1) / n)
+    res = {}
+    for name, (_, moved, launches) in forms.items():
+        ms = statistics.median(times[name])
+        res[name] = {"ms": round(ms, 5), "bytes": moved,
+                     "gbs": round(moved / (ms / 1e3) / 1e9, 1), "launches": launches,
+                     "reps": 3 * n}
     return res
 
 
@@ -592,12 +682,13 @@ def oracle_step(oracle, inp, F):
 
 def cpu_baseline(wl, W, layer, target_s=15.0):
     """Time the oracle (as it stands, all host cores it uses) on a bounded
-    sample of the same workload: the first `frac` of each op's rows.  The
-    outputs of the multi-core sample are then checked against the GPU's."""
+    sample of the same workload: the first `frac` of each op's rows, counted
+    in the step's algorithmic bytes.  The outputs of the multi-core sample are
+    then checked against the GPU's."""
     sys.path.insert(0, ROOT)
     import oracle
     h = layer.h_in
-    bts = step_bytes(wl, W)
+    bts = step_bytes(wl, W, layer.rope)
     total_bytes = sum(bts.values())
 
     def run(frac):
@@ -610,10 +701,7 @@ def cpu_baseline(wl, W, layer, target_s=15.0):
         dt_s = time.perf_counter() - t0
         last.clear()
         last.update(out)
-        sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S
-                   + 2 * bts["rope_rotate_half_q"] * tok / wl.S
-                   + bts["gelu_and_mul"] * rows_ff / wl.T_ff
-                   + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
+        sampled = sampled_bytes(bts, wl, tok, rows_ff, rows_n)
         return dt_s, sampled, (tok, rows_ff, rows_n)
 
     last = {}
@@ -706,8 +794,8 @@ def native(args):
         pg = tdist
     dt.load()
     wl = W.WORKLOADS[args.workload]
-    layer = Layer(wl, W, dev)
-    bts = step_bytes(wl, W)
+    layer = Layer(wl, W, dev, rope=args.rope)
+    bts = step_bytes(wl, W, args.rope)
     per_step = sum(bts.values())
 
     K = args.steps
@@ -721,9 +809,9 @@ def native(args):
     # MIN_DOM_LAUNCHES steps (median, min and max per call)
     g1 = step_graph(dt, layer, 1)
     gk = step_graph(dt, layer, K)
-    jd = OPS.index(DOMINANT)
+    jd = layer.ops.index(DOMINANT)
     KD = max(K, MIN_DOM_LAUNCHES)
-    dom_evs = timing_events(KD, (jd, jd + 1))
+    dom_evs = timing_events(KD, len(layer.ops), (jd, jd + 1))
     kern_evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(KD)]
     gd = step_graph(dt, layer, KD, dom_evs, kern_evs)
     sampler = ClockSampler(local)
@@ -766,10 +854,11 @@ def native(args):
     # beyond the step, on the same layer: RoPE on q and k in one in-place launch,
     # with the tables or with the angles evaluated inside the kernel
     fused = fused_rope_qk(dt, layer, wl, min(K, 200))
+    fused.update(rope_forms(dt, layer, wl, min(K, 200)))
     fused.update(geglu_prebuilt_table(dt, layer, wl, min(K, 200)))
 
     peak, peak_kind = peaks()
-    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak)
+    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak, args.rope)
     # the GEMM last: at the 1.1 kW power limit it leaves the GPU slower for a
     # while (memory-bound kernels timed right after it read 15-20% low)
     fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))
@@ -819,7 +908,7 @@ def native(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/gate/up/x, N(0,4) residual, N(1,0.1) w; "
                 "rotary angles from the token grid)",
-        "config": config_for(wl, per_step, f"replicas x{world}"),
+        "config": config_for(wl, per_step, f"replicas x{world}", args.rope),
         "pct_of_peak": round(100 * value / world / peak, 2),
         # the same against the part's nominal HBM3e bandwidth (7.7 TB/s, "~8 TB/s");
         # the >= 80% target is stated against the measured copy peak above (the
@@ -828,7 +917,7 @@ def native(args):
         # B*S over the layer's ops (the tables are once per forward), per-op times
         # from the breakdown pass; and B*S over the whole timed step
         "mtokens_per_s_per_layer": round(
-            tokens / (sum(kern_ms[o] for o in OPS[1:]) / 1e3) / 1e6, 3),
+            tokens / (sum(kern_ms[o] for o in layer.ops[1:]) / 1e3) / 1e6, 3),
         "mtokens_per_s_per_step": round(tokens / (ms_per_step / 1e3) / 1e6, 3),
         "mtokens_per_s_per_layer_with_next_rows": round(
             tokens / ((fused["rope_qk_inplace_angles"]["ms"] + kern_ms["gelu_and_mul"]
@@ -837,7 +926,7 @@ def native(args):
         "kernels": {op: {"ms": round(kern_ms[op], 5), "bytes": bts[op],
                          "gbs": round(bts[op] / (kern_ms[op] / 1e3) / 1e9, 1),
                          "frac_of_hbm_peak": round(bts[op] / (kern_ms[op] / 1e3) / 1e9 / peak, 4)}
-                    for op in OPS},
+                    for op in layer.ops},
         "kernels_how": (f"a separate graph of {KB} steps with CUDA events between all kernels; "
                         "the events cost time and stop consecutive launches from overlapping, "
                         "so these times add up to more than ms_per_step"),
@@ -867,7 +956,7 @@ def native(args):
         "launch": ("the K timed steps run as one CUDA graph (captured before timing; the "
                    "kernels' programmatic-dependent edges are kept inside it), replayed once "
                    "between two CUDA events"),
-        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "gpu_launches": launches_per_step(args.rope) * K,
         "next_rows": fused,
         "per_workload": per_wl,
         "clocks": clocks,
@@ -894,7 +983,7 @@ def reference(args):
     W = importlib.import_module(PKG + ".workloads")
     import oracle
     wl = W.WORKLOADS[args.workload]
-    bts = step_bytes(wl, W)
+    bts = step_bytes(wl, W, args.rope)
     steps, warm = args.steps, max(3, args.warmup)
     budget_s = 120.0
     F = wl.F
@@ -913,10 +1002,7 @@ def reference(args):
             "w": oracle.bf16_bits(W.normal_bf16((wl.C,), wl.seed, 6, mean=1.0,
                                                 std=math.sqrt(0.1))),
         }
-        sampled = (bts["rope_cos_sin_precompute"] * tok / wl.S
-                   + 2 * bts["rope_rotate_half_q"] * tok / wl.S
-                   + bts["gelu_and_mul"] * rows_ff / wl.T_ff
-                   + 2 * bts["rmsnorm_residual_attn"] * rows_n / wl.T_norm)
+        sampled = sampled_bytes(bts, wl, tok, rows_ff, rows_n)
         return data, sampled, (tok, rows_ff, rows_n)
 
     def one(d):
@@ -951,7 +1037,7 @@ def reference(args):
         "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * el / steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 (emulated in fp64)", "data": "synthetic",
-        "config": config_for(wl, sum(bts.values()), "host cores"),
+        "config": config_for(wl, sum(bts.values()), "host cores", args.rope),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

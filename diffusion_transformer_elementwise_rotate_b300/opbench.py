@@ -9,6 +9,7 @@ OP is one of
   tables      rope_cos_sin_precompute on the workload's (S, B, 1, rot) angles
   rope        rope_rotate_half on q (B, S, H, D), out of place
   rope_qk     rope_rotate_half_qk_ on q and k in place, from the tables
+  rope_qk_out rope_rotate_half_qk on q and k into separate outputs, from the tables
   rope_qk_angles   the same, cos/sin evaluated in the kernel from the angles
   geglu       gelu_and_mul on a (T, 2F) gate_up buffer (activation table + stream)
   geglu_table gelu_and_mul with a prebuilt activation table (the stream alone)
@@ -37,7 +38,8 @@ import torch
 from . import api as dt
 from . import workloads as W
 
-OPS = ("tables", "rope", "rope_qk", "rope_qk_angles", "geglu", "geglu_table", "rmsnorm", "gemm")
+OPS = ("tables", "rope", "rope_qk", "rope_qk_out", "rope_qk_angles", "geglu", "geglu_table",
+       "rmsnorm", "gemm")
 
 
 def _normal(shape, dev, g, mean=0.0, std=1.0):
@@ -50,7 +52,7 @@ def setup(op: str, wl: W.Workload, rows: int | None, dev):
     """(callable running one launch of the op, algorithmic bytes or flops, unit,
     description, live tensors)."""
     g = torch.Generator(device=dev).manual_seed(0)
-    if op in ("tables", "rope", "rope_qk", "rope_qk_angles"):
+    if op in ("tables", "rope", "rope_qk", "rope_qk_out", "rope_qk_angles"):
         S = wl.S if rows is None else min(wl.S, max(1, rows // wl.B))
         freqs = W.freqs_for(wl)[:S].contiguous().to(dev)
         B, H, D, R = wl.B, wl.H, wl.D, wl.rot
@@ -68,6 +70,12 @@ def setup(op: str, wl: W.Workload, rows: int | None, dev):
                     f"rope_rotate_half x ({B}, {S}, {H}, {D}) rot {R}, out of place",
                     (freqs, cos, sin, q, out))
         k = _normal((B, S, H, D), dev, g)
+        if op == "rope_qk_out":
+            qo, ko = torch.empty_like(q), torch.empty_like(k)
+            return (lambda: dt.rope_rotate_half_qk(q, k, cos=cos, sin=sin, q_out=qo, k_out=ko),
+                    8 * tok * H * D + 4 * tok * R, "B",
+                    f"rope_rotate_half_qk q, k ({B}, {S}, {H}, {D}) rot {R}, out of place, "
+                    "tables", (freqs, cos, sin, q, k, qo, ko))
         moved = 4 * tok * 2 * H * R + 4 * tok * R
         if op == "rope_qk":
             return (lambda: dt.rope_rotate_half_qk_(q, k, cos=cos, sin=sin), moved, "B",

@@ -176,6 +176,8 @@ def algorithmic_bytes(wl: Workload) -> dict:
     return {
         "rope_cos_sin_precompute": wl.tokens * wl.rot * (4 + 2 + 2),
         "rope_rotate_half": 4 * wl.tokens * wl.H * wl.D + 4 * wl.tokens * wl.rot,
+        # q and k in one out-of-place launch: the tables are read once for both
+        "rope_rotate_half_qk": 8 * wl.tokens * wl.H * wl.D + 4 * wl.tokens * wl.rot,
         "gelu_and_mul": 6 * wl.T_ff * wl.F,
         "rmsnorm_residual": 8 * wl.T_norm * wl.C + 2 * wl.C,
     }
