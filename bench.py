@@ -43,23 +43,26 @@ NOMINAL_HBM_GBS = 7700.0
 # of the tables.
 ROPE_FORMS = {"qk": ["rope_rotate_half_qk"],
               "separate": ["rope_rotate_half_q", "rope_rotate_half_k"]}
+# Made once per forward and used by every layer: the cos/sin tables and the
+# GEGLU activation table.  In the timed step they run on a side branch of the
+# graph, beside the pre-attention norm, which does not depend on them.
+PER_FORWARD = ("rope_cos_sin_precompute", "gelu_table_build")
 DOMINANT = "gelu_and_mul"
 MIN_DOM_LAUNCHES = 20  # the dominant kernel's roofline is the median of at least this many calls
 PER_WORKLOAD = ("image", "cfg")  # other layer shapes reported beside the headline layer
 
 
 def step_ops(rope="qk"):
-    """The step's calls in order (each a range between two timing events)."""
-    return (["rope_cos_sin_precompute"] + ROPE_FORMS[rope]
-            + ["gelu_and_mul", "rmsnorm_residual_attn", "rmsnorm_residual_ffn"])
+    """The step's calls in the order of a Pre-Norm layer, after the per-forward
+    tables: pre-attention norm, RoPE on q and k, pre-FFN norm, GEGLU (its
+    streaming kernel on the table built above).  One kernel each."""
+    return (list(PER_FORWARD) + ["rmsnorm_residual_attn"] + ROPE_FORMS[rope]
+            + ["rmsnorm_residual_ffn", "gelu_and_mul"])
 
 
 def launches_per_step(rope="qk"):
-    """Kernels per step: one per call, and two for GEGLU (activation table and
-    streaming kernel)."""
-    return len(step_ops(rope)) + 1
-
-
+    """Kernels per step: one per call."""
+    return len(step_ops(rope))
 
 
 def config_for(wl, per_step, parallelism, rope="qk"):
@@ -69,9 +72,9 @@ def config_for(wl, per_step, parallelism, rope="qk"):
                      f"split {'/'.join(map(str, wl.split))}; GEGLU ({wl.T_ff}, 2x{wl.F}); "
                      f"RMSNorm+residual ({wl.T_norm}, {wl.C}) x2; cos/sin tables "
                      f"({wl.tokens}, {wl.rot})"),
-        "step": ("tables + RoPE q and k (one launch, out of place) + GEGLU + 2x RMSNorm+residual"
-                 if rope == "qk" else
-                 "tables + RoPE q + RoPE k + GEGLU + 2x RMSNorm+residual"),
+        "step": ("cos/sin and GEGLU activation tables + RMSNorm+residual (attention) + "
+                 + ("RoPE q and k (one launch, out of place)" if rope == "qk" else
+                    "RoPE q + RoPE k") + " + RMSNorm+residual (FFN) + GEGLU"),
         "bytes_per_step": per_step,
         "l2": "inputs larger than L2 (126 MB) for every kernel; no flush",
         "parallelism": parallelism,
@@ -89,6 +92,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rope", default="qk", choices=sorted(ROPE_FORMS),
                     help="RoPE on q and k in one launch (qk) or one call per tensor (separate)")
+    ap.add_argument("--serial", action="store_true",
+                    help="run the timed step's calls one after another on one stream (by "
+                         "default the per-forward tables run beside the pre-attention norm)")
     return ap.parse_args()
 
 
@@ -140,6 +146,7 @@ def step_bytes(wl, W, rope="qk"):
     b = W.algorithmic_bytes(wl)
     per_op = {
         "rope_cos_sin_precompute": b["rope_cos_sin_precompute"],
+        "gelu_table_build": b["gelu_table_build"],
         "rope_rotate_half_qk": b["rope_rotate_half_qk"],
         "rope_rotate_half_q": b["rope_rotate_half"],
         "rope_rotate_half_k": b["rope_rotate_half"],
@@ -153,9 +160,10 @@ def step_bytes(wl, W, rope="qk"):
 def sampled_bytes(bts, wl, tok, rows_ff, rows_n):
     """The algorithmic bytes of the step on a sample of the layer: the first
     `tok` positions for the tables and RoPE, `rows_ff` GEGLU rows and `rows_n`
-    rows of each RMSNorm (every op's bytes are proportional to its rows)."""
+    rows of each RMSNorm (every op's bytes are proportional to its rows; the
+    GEGLU activation table is whole in any sample)."""
     frac = {"gelu_and_mul": rows_ff / wl.T_ff, "rmsnorm_residual_attn": rows_n / wl.T_norm,
-            "rmsnorm_residual_ffn": rows_n / wl.T_norm}
+            "rmsnorm_residual_ffn": rows_n / wl.T_norm, "gelu_table_build": 1.0}
     return sum(v * frac.get(op, tok / wl.S) for op, v in bts.items())
 
 
@@ -267,9 +275,10 @@ class ClockSampler:
 class Layer:
     """One layer's tensors on the device plus pinned host copies."""
 
-    def __init__(self, wl, W, dev, keep_host=True, rope="qk"):
+    def __init__(self, wl, W, dev, keep_host=True, rope="qk", serial=False):
         self.wl = wl
         self.rope = rope
+        self.serial = serial
         self.ops = step_ops(rope)
         pin = torch.cuda.is_available() and keep_host
         self.h_in = {
@@ -286,7 +295,11 @@ class Layer:
         e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)  # noqa: E731
         self.d.update({"cos": e((B * S, wl.rot)), "sin": e((B * S, wl.rot)),
                        "q_out": e((B, S, H, D)), "k_out": e((B, S, H, D)),
-                       "ff_out": e((wl.T_ff, F)), "y1": e((T, C)), "y2": e((T, C))})
+                       "ff_out": e((wl.T_ff, F)), "y1": e((T, C)), "y2": e((T, C)),
+                       "gelu_table": torch.empty(W.GELU_TABLE_BYTES, dtype=torch.uint8,
+                                                 device=dev)})
+        # the side branch of the per-forward tables
+        self.side = torch.cuda.Stream(device=dev) if torch.cuda.is_available() else None
         self.out_names = ["cos", "sin", "q_out", "k_out", "ff_out", "y1", "y2", "r1", "r2"]
         if not keep_host:
             self.h_in, self.h_out = {}, {}
@@ -299,28 +312,21 @@ class Layer:
         pipelining host transfers of one step against the compute of another."""
         return {k: torch.empty_like(v) for k, v in self.d.items()}
 
-    def step(self, dt, ev=None, d=None, geglu_kernel_ev=None):
-        """One layer step.  ev: len(self.ops) + 1 events (or None) for the
-        boundaries around the calls.  geglu_kernel_ev: an event to record
-        between GEGLU's two launches; the call is then made as its two C-ABI
-        halves (build the activation table into the same per-stream workspace,
-        then the streaming kernel on it), the very kernels dtrot_gelu_and_mul
-        launches."""
+    def step(self, dt, ev=None, d=None, serial=None):
+        """One layer step.  By default the per-forward tables (cos/sin and the
+        GEGLU activation table) run on a side stream that forks from the
+        current one at the start of the step, beside the pre-attention norm,
+        and joins it before the RoPE; the rest runs in order on the current
+        stream.  With `serial`, or with `ev` (len(self.ops) + 1 events, or
+        None, recorded at the boundaries between the calls), every call runs
+        in order on the current stream."""
         d, F = (self.d if d is None else d), self.wl.F
-
-        def geglu():
-            gate, up = d["gate_up"][:, :F], d["gate_up"][:, F:]
-            if geglu_kernel_ev is None:
-                dt.gelu_and_mul(gate, up, out=d["ff_out"])
-            else:
-                st = torch.cuda.current_stream(gate.device).cuda_stream
-                ws = dt.gelu_table_build(dt.gelu_workspace(gate.device, st))
-                geglu_kernel_ev.record()
-                dt.gelu_and_mul(gate, up, out=d["ff_out"], table=ws)
-
+        serial = self.serial if serial is None else serial
+        gate, up = d["gate_up"][:, :F], d["gate_up"][:, F:]
         calls = {
             "rope_cos_sin_precompute":
                 lambda: dt.rope_cos_sin_precompute(d["freqs"], d["cos"], d["sin"]),
+            "gelu_table_build": lambda: dt.gelu_table_build(d["gelu_table"]),
             "rope_rotate_half_qk":
                 lambda: dt.rope_rotate_half_qk(d["q"], d["k"], cos=d["cos"], sin=d["sin"],
                                                q_out=d["q_out"], k_out=d["k_out"]),
@@ -328,18 +334,31 @@ class Layer:
                 lambda: dt.rope_rotate_half(d["q"], d["cos"], d["sin"], out=d["q_out"]),
             "rope_rotate_half_k":
                 lambda: dt.rope_rotate_half(d["k"], d["cos"], d["sin"], out=d["k_out"]),
-            "gelu_and_mul": geglu,
+            "gelu_and_mul": lambda: dt.gelu_and_mul(gate, up, out=d["ff_out"],
+                                                    table=d["gelu_table"]),
             "rmsnorm_residual_attn":
                 lambda: dt.rmsnorm_residual(d["x1"], d["r1"], d["w"], 1e-6, out=d["y1"]),
             "rmsnorm_residual_ffn":
                 lambda: dt.rmsnorm_residual(d["x2"], d["r2"], d["w"], 1e-6, out=d["y2"]),
         }
-        for i, op in enumerate(self.ops):
-            if ev is not None and ev[i] is not None:
-                ev[i].record()
+        if ev is not None or serial:
+            for i, op in enumerate(self.ops):
+                if ev is not None and ev[i] is not None:
+                    ev[i].record()
+                calls[op]()
+            if ev is not None and ev[len(self.ops)] is not None:
+                ev[len(self.ops)].record()
+            return
+        cur = torch.cuda.current_stream()
+        self.side.wait_stream(cur)  # the tables are rewritten after the last step's readers
+        with torch.cuda.stream(self.side):
+            for op in PER_FORWARD:
+                calls[op]()
+        rest = [op for op in self.ops if op not in PER_FORWARD]
+        for op in rest:
+            if op.startswith("rope_"):
+                cur.wait_stream(self.side)  # the RoPE reads the cos/sin tables
             calls[op]()
-        if ev is not None and ev[len(self.ops)] is not None:
-            ev[len(self.ops)].record()
 
     def h2d(self, d=None):
         d = self.d if d is None else d
@@ -354,25 +373,25 @@ class Layer:
         return sum(self.h_out[k].numel() * self.h_out[k].element_size() for k in self.out_names)
 
 
-def step_graph(dt, layer, steps, evs=None, kevs=None):
-    """A CUDA graph of `steps` layer steps (evs[i]: the 7 events of step i, or
-    None; kevs[i]: an event between GEGLU's two launches in step i, or None).  The steps' kernels keep their programmatic-dependent edges inside
-    the graph, and replaying it costs one host call, so the timed passes measure
+def step_graph(dt, layer, steps, evs=None):
+    """A CUDA graph of `steps` layer steps (evs[i]: the events of step i, or
+    None).  The steps' kernels keep their programmatic-dependent edges inside
+    the graph, and the side branch of the per-forward tables becomes a parallel
+    branch of it; replaying it costs one host call, so the timed passes measure
     the GPU alone, not the Python launch path (on a busy host that path could
     fall behind the short kernels).  Events given are external: they become
     event-record nodes whose times elapsed_time() reads after a replay."""
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
+    warm = torch.cuda.Stream()
+    warm.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(warm):
         for _ in range(2):
             layer.step(dt)
-    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.current_stream().wait_stream(warm)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for i in range(steps):
-            layer.step(dt, None if evs is None else evs[i],
-                       geglu_kernel_ev=None if kevs is None else kevs[i])
+            layer.step(dt, None if evs is None else evs[i])
     torch.cuda.synchronize()
     return g
 
@@ -416,7 +435,7 @@ def timed_steps(dt, layer, steps, warm):
     return ms
 
 
-def other_workloads(dt, W, dev, steps, peak, rope="qk"):
+def other_workloads(dt, W, dev, steps, peak, rope="qk", serial=False):
     """The image and CFG layers: the same step on their shapes, timed like the
     headline layer (a pass of plain steps, then a pass with events between the
     kernels for the per-op figures), each on its own tensors.  Their steps move
@@ -425,7 +444,7 @@ def other_workloads(dt, W, dev, steps, peak, rope="qk"):
     res = {}
     for name in PER_WORKLOAD:
         wl = W.WORKLOADS[name]
-        layer = Layer(wl, W, dev, keep_host=False, rope=rope)
+        layer = Layer(wl, W, dev, keep_host=False, rope=rope, serial=serial)
         bts = step_bytes(wl, W, rope)
         per_step = sum(bts.values())
         ms = timed_steps(dt, layer, steps, 3) / steps
@@ -438,7 +457,8 @@ def other_workloads(dt, W, dev, steps, peak, rope="qk"):
             "gbs": round(per_step / (ms / 1e3) / 1e9, 1),
             "frac_of_hbm_peak": round(per_step / (ms / 1e3) / 1e9 / peak, 4),
             "mtokens_per_s_per_layer": round(
-                tokens / (sum(km[o] for o in layer.ops[1:]) / 1e3) / 1e6, 3),
+                tokens / (sum(km[o] for o in layer.ops if o not in PER_FORWARD) / 1e3)
+                / 1e6, 3),
             "mtokens_per_s_per_step": round(tokens / (ms / 1e3) / 1e6, 3),
             "kernels": {op: {"ms": round(km[op], 5), "bytes": bts[op],
                              "gbs": round(bts[op] / (km[op] / 1e3) / 1e9, 1),
@@ -794,7 +814,7 @@ def native(args):
         pg = tdist
     dt.load()
     wl = W.WORKLOADS[args.workload]
-    layer = Layer(wl, W, dev, rope=args.rope)
+    layer = Layer(wl, W, dev, rope=args.rope, serial=args.serial)
     bts = step_bytes(wl, W, args.rope)
     per_step = sum(bts.values())
 
@@ -804,16 +824,15 @@ def native(args):
     # the K timed steps as one graph with no events between kernels (an event
     # between two launches costs ~2 us and stops the second from starting as
     # the programmatic dependent of the first); the dominant kernel with events
-    # around its call (both of its launches, the activation table and the
-    # streaming kernel) in every step of a second graph of at least
-    # MIN_DOM_LAUNCHES steps (median, min and max per call)
+    # around it and around the activation-table launch, in every step of a
+    # second graph of at least MIN_DOM_LAUNCHES steps whose calls run one after
+    # another (median, min and max per launch)
     g1 = step_graph(dt, layer, 1)
     gk = step_graph(dt, layer, K)
-    jd = layer.ops.index(DOMINANT)
+    jt, jd = layer.ops.index("gelu_table_build"), layer.ops.index(DOMINANT)
     KD = max(K, MIN_DOM_LAUNCHES)
-    dom_evs = timing_events(KD, len(layer.ops), (jd, jd + 1))
-    kern_evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(KD)]
-    gd = step_graph(dt, layer, KD, dom_evs, kern_evs)
+    dom_evs = timing_events(KD, len(layer.ops), (jt, jt + 1, jd, jd + 1))
+    gd = step_graph(dt, layer, KD, dom_evs)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
@@ -837,11 +856,12 @@ def native(args):
     gd.replay()
     torch.cuda.synchronize()
     clocks = sampler.stop() if rank == 0 else None
-    # the dominant kernel (GEGLU's streaming launch) and its whole call (with the
-    # activation-table launch before it)
-    dom_all = sorted(kern_evs[i].elapsed_time(dom_evs[i][jd + 1]) for i in range(KD))
+    # the dominant kernel (GEGLU's streaming launch) and the whole GEGLU work
+    # of a step (the activation-table launch and the streaming launch)
+    dom_all = sorted(dom_evs[i][jd].elapsed_time(dom_evs[i][jd + 1]) for i in range(KD))
     dom_ms = statistics.median(dom_all)
-    call_all = sorted(dom_evs[i][jd].elapsed_time(dom_evs[i][jd + 1]) for i in range(KD))
+    call_all = sorted(dom_evs[i][jt].elapsed_time(dom_evs[i][jt + 1])
+                      + dom_evs[i][jd].elapsed_time(dom_evs[i][jd + 1]) for i in range(KD))
     call_ms = statistics.median(call_all)
     del g1, gk, gd
     # per-op breakdown: a separate graph with events between all kernels
@@ -858,7 +878,7 @@ def native(args):
     fused.update(geglu_prebuilt_table(dt, layer, wl, min(K, 200)))
 
     peak, peak_kind = peaks()
-    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak, args.rope)
+    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak, args.rope, args.serial)
     # the GEMM last: at the 1.1 kW power limit it leaves the GPU slower for a
     # while (memory-bound kernels timed right after it read 15-20% low)
     fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))
@@ -917,7 +937,8 @@ def native(args):
         # B*S over the layer's ops (the tables are once per forward), per-op times
         # from the breakdown pass; and B*S over the whole timed step
         "mtokens_per_s_per_layer": round(
-            tokens / (sum(kern_ms[o] for o in layer.ops[1:]) / 1e3) / 1e6, 3),
+            tokens / (sum(kern_ms[o] for o in layer.ops if o not in PER_FORWARD) / 1e3)
+            / 1e6, 3),
         "mtokens_per_s_per_step": round(tokens / (ms_per_step / 1e3) / 1e6, 3),
         "mtokens_per_s_per_layer_with_next_rows": round(
             tokens / ((fused["rope_qk_inplace_angles"]["ms"] + kern_ms["gelu_and_mul"]
@@ -939,12 +960,12 @@ def native(args):
                      "call_achieved": round(bts[DOMINANT] / (call_ms / 1e3) / 1e9, 1),
                      "how": (f"median over {KD} launches of the time between CUDA events around "
                              "the streaming kernel, in every step of a graph of the same layer "
-                             "steps replayed after the timed ones; there the call is made as its "
-                             "two C-ABI halves (the activation table into the same workspace, "
-                             "then the streaming kernel on it: the kernels gelu_and_mul "
-                             "launches) with an event between them; call_ms brackets both "
-                             "launches; the events also keep the kernel from overlapping its "
-                             "neighbours, which the unbracketed timed steps allow"),
+                             "steps replayed after the timed ones, with the step's calls one "
+                             "after another; call_ms adds the activation-table launch of the "
+                             "same step, bracketed the same way (the two launches "
+                             "dtrot_gelu_and_mul makes); the events also keep the kernels from "
+                             "overlapping their neighbours, which the unbracketed timed steps "
+                             "allow"),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
                      "algorithmic_bytes": bts[DOMINANT]},
@@ -955,7 +976,11 @@ def native(args):
                        "three streams with two device sets"},
         "launch": ("the K timed steps run as one CUDA graph (captured before timing; the "
                    "kernels' programmatic-dependent edges are kept inside it), replayed once "
-                   "between two CUDA events"),
+                   "between two CUDA events; "
+                   + ("every call of a step in order on one stream" if args.serial else
+                      "in each step the per-forward tables (cos/sin, GEGLU activation) run on "
+                      "a parallel branch beside the pre-attention norm and join before the "
+                      "RoPE")),
         "gpu_launches": launches_per_step(args.rope) * K,
         "next_rows": fused,
         "per_workload": per_wl,

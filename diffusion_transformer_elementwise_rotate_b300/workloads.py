@@ -171,9 +171,14 @@ def shard_rows(n: int, rank: int, world: int) -> tuple:
     return lo, lo + base + (1 if rank < extra else 0)
 
 
+# the GEGLU activation table: one bf16 entry per bf16 gate value
+GELU_TABLE_BYTES = 2 * 65536
+
+
 def algorithmic_bytes(wl: Workload) -> dict:
     """Bytes each op must move at minimum (read inputs once, write outputs once)."""
     return {
+        "gelu_table_build": GELU_TABLE_BYTES,
         "rope_cos_sin_precompute": wl.tokens * wl.rot * (4 + 2 + 2),
         "rope_rotate_half": 4 * wl.tokens * wl.H * wl.D + 4 * wl.tokens * wl.rot,
         # q and k in one out-of-place launch: the tables are read once for both
