@@ -139,6 +139,26 @@ __device__ __forceinline__ double block_sum_double(RowShared& sh, double v) {
     return t;
 }
 
+// Warp-wide versions for rows that one warp owns: the xor butterfly merges
+// the same two values at every step (the merge is symmetric in its operands),
+// so every lane ends with the same bits.
+__device__ __forceinline__ bool warp_sumsq(float hi, float lo, float& tot_hi, float& tot_lo) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        acc_merge(hi, lo, h2, l2);
+    }
+    fast_two_sum(hi, lo, tot_hi, tot_lo);
+    return (tot_hi <= 1e37f) && (tot_hi >= 0x1p-60f);  // false for NaN too
+}
+
+__device__ __forceinline__ double warp_sum_double(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 __device__ __forceinline__ void inv_from_double(double total, int64_t C, float eps,
                                                 float& inv_hi, float& inv_lo) {
     const double inv = 1.0 / sqrt(total / (double)C + (double)eps);
@@ -199,16 +219,18 @@ __device__ __forceinline__ double sq_d2(uint32_t h2) {
 
 // Row statistics: inv = (mean(h^2) + eps)^(-1/2) as a double-float, from the
 // thread's compensated partial sum; `redo_sq` recomputes the thread's partial
-// in double when the fp32 total is out of range (uniform across the block).
-template <typename RedoSq>
-__device__ __forceinline__ void row_inv(RowShared& sh, int slot, float hi, float lo, int64_t C,
+// in double when the fp32 total is out of range (uniform across the row's
+// threads).  WARP: the row belongs to one warp (sh is not used).
+template <bool WARP, typename RedoSq>
+__device__ __forceinline__ void row_inv(RowShared* sh, int slot, float hi, float lo, int64_t C,
                                         float eps, RedoSq redo_sq, float& inv_hi,
                                         float& inv_lo) {
     float th, tl;
-    if (block_sumsq(sh, slot, hi, lo, th, tl) && C < (1 << 24)) {
+    const bool ok = WARP ? warp_sumsq(hi, lo, th, tl) : block_sumsq(*sh, slot, hi, lo, th, tl);
+    if (ok && C < (1 << 24)) {
         inv_rms_df(th, tl, C, eps, inv_hi, inv_lo);
     } else {
-        const double t = block_sum_double(sh, redo_sq());
+        const double t = WARP ? warp_sum_double(redo_sq()) : block_sum_double(*sh, redo_sq());
         inv_from_double(t, C, eps, inv_hi, inv_lo);
     }
 }
@@ -261,15 +283,25 @@ __device__ __forceinline__ bool y_settled(float y) {
     return (a >= 0x1p-90f) && (a <= 0x1p100f) && !mid;
 }
 
-// One token row on the vector path.  Thread t owns the 8-column vectors
-// v = k * blockDim + t (k < VPT, v < nv); xc, rc hold its x and residual
-// vectors of the row and wv its w vectors.  FULL: nv == VPT * blockDim (every
-// thread owns VPT vectors, so no access needs a bounds check).
-template <int VPT, bool FULL>
-__device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int slot, int64_t row,
+// The 8-column vectors of a row that a thread owns: v = k * row_stride + idx
+// for k < VPT (and v < nv), the row spread over the CTA (idx = thread) or,
+// WARP, over one warp (idx = lane).
+template <bool WARP>
+__device__ __forceinline__ int row_idx() { return WARP ? (int)(threadIdx.x & 31) : (int)threadIdx.x; }
+template <bool WARP>
+__device__ __forceinline__ int row_stride() { return WARP ? 32 : (int)blockDim.x; }
+
+// One token row on the vector path.  The thread owns the vectors
+// v = k * row_stride + row_idx (k < VPT, v < nv); xc, rc hold its x and
+// residual vectors of the row and wv its w vectors.  FULL: nv == VPT *
+// row_stride (every thread owns VPT vectors, so no access needs a bounds
+// check).
+template <int VPT, bool FULL, bool WARP>
+__device__ __forceinline__ void rms_row(const RmsParams& p, RowShared* sh, int slot, int64_t row,
                                         int nv, const uint4 (&xc)[VPT], const uint4 (&rc)[VPT],
                                         const uint4 (&wv)[VPT]) {
-    const int tid = threadIdx.x;
+    const int tid = row_idx<WARP>();
+    const int stride = row_stride<WARP>();
     // h = RN16(x + r), written back to the residual stream; exact squares
     // accumulated lane-wise with TwoSum
     uint4 hv[VPT];
@@ -277,7 +309,7 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
     uint4* rrow = reinterpret_cast<uint4*>(p.residual + row * p.sr);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-        const int v = k * (int)blockDim.x + tid;
+        const int v = k * stride + tid;
         if (FULL || v < nv) {
             hv[k].x = badd2(xc[k].x, rc[k].x);
             hv[k].y = badd2(xc[k].y, rc[k].y);
@@ -299,12 +331,12 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
     acc_merge(shi, slo, f2hi(hi), f2hi(lo));
 
     float inv_hi, inv_lo;
-    row_inv(sh, slot, shi, slo, p.C, p.eps,
+    row_inv<WARP>(sh, slot, shi, slo, p.C, p.eps,
             [&]() {
                 double d = 0.0;
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    const int v = k * (int)blockDim.x + tid;
+                    const int v = k * stride + tid;
                     if (FULL || v < nv)
                         d += sq_d2(hv[k].x) + sq_d2(hv[k].y) + sq_d2(hv[k].z) + sq_d2(hv[k].w);
                 }
@@ -322,7 +354,7 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
     uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.so);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-        const int v = k * (int)blockDim.x + tid;
+        const int v = k * stride + tid;
         if (FULL || v < nv) {
             const uint32_t hw[4] = {hv[k].x, hv[k].y, hv[k].z, hv[k].w};
             const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
@@ -341,12 +373,28 @@ __device__ __forceinline__ void rms_row(const RmsParams& p, RowShared& sh, int s
     }
 }
 
-template <int VPT, bool FULL>
+template <int VPT, bool FULL, bool WARP>
 __device__ __forceinline__ void load_w(const RmsParams& p, int nv, uint4 (&wv)[VPT]) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-        const int v = k * (int)blockDim.x + threadIdx.x;
+        const int v = k * row_stride<WARP>() + row_idx<WARP>();
         if (FULL || v < nv) wv[k] = __ldg(reinterpret_cast<const uint4*>(p.w) + v);
+    }
+}
+
+// A row's x and residual vectors into registers.
+template <int VPT, bool FULL, bool WARP>
+__device__ __forceinline__ void load_row(const RmsParams& p, int nv, int64_t r, uint4 (&xs)[VPT],
+                                         uint4 (&rs)[VPT]) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + r * p.sx);
+    const uint4* rr = reinterpret_cast<const uint4*>(p.residual + r * p.sr);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * row_stride<WARP>() + row_idx<WARP>();
+        if (FULL || v < nv) {
+            xs[k] = xr[v];
+            rs[k] = rr[v];
+        }
     }
 }
 
@@ -369,29 +417,48 @@ __global__ void __launch_bounds__(rms_max_threads(VPT), rms_min_blocks(VPT))
     __shared__ RowShared sh;
     pdl_wait();
     const int nv = (int)(p.C >> 3);
-    const int tid = threadIdx.x;
     uint4 wv[VPT], xc[VPT], rc[VPT];
-    load_w<VPT, FULL>(p, nv, wv);
-    auto load_row = [&](int64_t r, uint4 (&xs)[VPT], uint4 (&rs)[VPT]) {
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x + r * p.sx);
-        const uint4* rr = reinterpret_cast<const uint4*>(p.residual + r * p.sr);
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * (int)blockDim.x + tid;
-            if (FULL || v < nv) {
-                xs[k] = xr[v];
-                rs[k] = rr[v];
-            }
-        }
-    };
+    load_w<VPT, FULL, false>(p, nv, wv);
     int64_t row = blockIdx.x;
-    if (row < p.T) load_row(row, xc, rc);
+    if (row < p.T) load_row<VPT, FULL, false>(p, nv, row, xc, rc);
     int slot = 0;
     for (; row < p.T; row += gridDim.x, slot ^= 1) {
         uint4 xn[VPT], rn[VPT];
         const int64_t nrow = row + gridDim.x;
-        if (nrow < p.T) load_row(nrow, xn, rn);
-        rms_row<VPT, FULL>(p, sh, slot, row, nv, xc, rc, wv);
+        if (nrow < p.T) load_row<VPT, FULL, false>(p, nv, nrow, xn, rn);
+        rms_row<VPT, FULL, false>(p, &sh, slot, row, nv, xc, rc, wv);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            xc[k] = xn[k];
+            rc[k] = rn[k];
+        }
+    }
+}
+
+// Narrow rows (at most 32 * VPT vectors): one warp per row, so the row's sum
+// needs shuffles only, no shared memory and no barrier; the warps of a CTA
+// work on different rows independently.  Persistent warps, each prefetching
+// its next row like the CTA-wide kernel, in CTAs of 4 warps.  Measured per
+// call at ~1.34 GB (32 * VPT a multiple of C / 8 or not): C = 768 225 us and
+// C = 1024 215 us against 288 and 277 us with a CTA per row.  The variant
+// without bounds checks for rows that fill the warp, and 8-warp CTAs, were
+// slower at some widths (C = 768: 452 us), so every width takes this one.
+constexpr int kWarpRowThreads = 128;
+
+template <int VPT>
+__global__ void __launch_bounds__(kWarpRowThreads) rms_warp_kernel(RmsParams p) {
+    pdl_wait();
+    const int nv = (int)(p.C >> 3);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    uint4 wv[VPT], xc[VPT], rc[VPT];
+    load_w<VPT, false, true>(p, nv, wv);
+    int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row < p.T) load_row<VPT, false, true>(p, nv, row, xc, rc);
+    for (; row < p.T; row += warps) {
+        uint4 xn[VPT], rn[VPT];
+        const int64_t nrow = row + warps;
+        if (nrow < p.T) load_row<VPT, false, true>(p, nv, nrow, xn, rn);
+        rms_row<VPT, false, true>(p, nullptr, 0, row, nv, xc, rc, wv);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             xc[k] = xn[k];
@@ -418,7 +485,7 @@ __global__ void __launch_bounds__(256) rms_generic_kernel(RmsParams p) {
             acc_add(hi, lo, __fmul_rn(hf, hf));
         }
         float inv_hi, inv_lo;
-        row_inv(sh, slot, hi, lo, p.C, p.eps,
+        row_inv<false>(&sh, slot, hi, lo, p.C, p.eps,
                 [&]() {
                     double d = 0.0;
                     for (int64_t c = threadIdx.x; c < p.C; c += blockDim.x) {
@@ -462,6 +529,20 @@ cudaError_t launch_vec(const RmsParams& p, int threads, cudaStream_t st) {
                                                : launch_vec_as<VPT, false>(p, threads, st);
 }
 
+template <int VPT>
+cudaError_t launch_warp(const RmsParams& p, cudaStream_t st) {
+    // persistent warps: as many CTAs as fit on the device, at most one warp per row
+    int per_sm = 0;
+    cudaError_t e = per_sm_blocks(rms_warp_kernel<VPT>, kWarpRowThreads, 0, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t rows_per_cta = kWarpRowThreads / 32;
+    int64_t blocks = (int64_t)num_sms() * per_sm;
+    const int64_t need = (p.T + rows_per_cta - 1) / rows_per_cta;
+    if (blocks > need) blocks = need;
+    return launch_pdl(rms_warp_kernel<VPT>, dim3((unsigned)blocks), dim3(kWarpRowThreads), 0,
+                      st, p);
+}
+
 }  // namespace
 
 cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st) {
@@ -469,6 +550,16 @@ cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st) {
                      aligned(p.x, 16) && aligned(p.residual, 16) && aligned(p.w, 16) &&
                      aligned(p.out, 16);
     const int64_t nv = p.C / 8;
+    // rows of at most 128 vectors (C <= 1024): one warp per row, VPT = nv / 32
+    // rounded up
+    if (vec && nv <= 4 * 32) {
+        switch ((nv + 31) / 32) {
+            case 1: return launch_warp<1>(p, st);
+            case 2: return launch_warp<2>(p, st);
+            case 3: return launch_warp<3>(p, st);
+            default: return launch_warp<4>(p, st);
+        }
+    }
     // VPT vectors per thread: the smallest of 1, 2, 4 that keeps a row within
     // 160 threads, else 8 (up to 256 threads, C <= 16384)
     if (vec && nv <= 8 * 256) {

@@ -552,8 +552,10 @@ def test_rmsnorm_sweep(C):
     _rms_check(x, r, w, None, f"C={C}")
 
 
-def test_rmsnorm_special_rows():
-    C = 256
+@pytest.mark.parametrize("C", [256, 1000, 5120])
+def test_rmsnorm_special_rows(C):
+    # one warp per row (C = 256: full rows; 1000: 4 vectors per lane, the last
+    # partial) and one CTA per row (5120)
     x = W.normal_bf16((8, C), 5, 4)
     r = torch.zeros((8, C), dtype=torch.bfloat16)
     x[1] = 0                      # all-zero row: y = 0
@@ -565,6 +567,17 @@ def test_rmsnorm_special_rows():
     x[7] *= 2.0 ** -130           # subnormal inputs
     w = W.normal_bf16((C,), 5, 6, mean=1.0, std=0.316)
     _rms_check(x, r, w, None, "special rows")
+
+
+# Rows of at most 128 vectors of 8 take the one-warp-per-row kernel with 1-4
+# vectors per lane, filling the warp or not; 1032 is the first width past it.
+@pytest.mark.parametrize("C", [136, 264, 512, 520, 1000, 1024, 1032])
+def test_rmsnorm_warp_rows(C):
+    T = 2053
+    x = W.normal_bf16((T, C), 90 + C, 4)
+    r = W.normal_bf16((T, C), 90 + C, 5, std=2.0)
+    w = W.normal_bf16((C,), 90 + C, 6, mean=1.0, std=0.316)
+    _rms_check(x, r, w, None, f"C={C}")
 
 
 def test_rmsnorm_row_subsets_and_x_is_residual():
