@@ -36,6 +36,7 @@ namespace dtrot {
 namespace {
 
 constexpr int kMaxRot = 256;  // angle-mode fast path: rot_dim <= kMaxRot
+constexpr int kAngIt = kMaxRot / 64;  // first-half angle columns per lane (32 lanes)
 constexpr int kWarps = 8;     // warps per CTA of the fast kernel
 
 template <int VW>
@@ -139,20 +140,34 @@ __global__ void __launch_bounds__(kWarps * 32) rope_qk_kernel(QKArgs a) {
             // angle with the same bits has the same entry, which is copied
             // (per-axis rotate-half angles repeat their half-row); any other
             // is evaluated
+            // a lane's angles (at most kAngIt columns and their partners) are
+            // all loaded before any is evaluated, so it waits for memory once
             const float* fr = p.freqs + (s * p.B + b) * p.rot;
-            for (int64_t c = lane; c < hh; c += 32) {
-                const float f1 = __ldg(fr + c), f2 = __ldg(fr + c + hh);
-                uint16_t cv, sv;
-                cos_sin_entry(f1, cv, sv);
-                cs[w][0][c] = cv;
-                cs[w][1][c] = sv;
-                if (__float_as_uint(f2) != __float_as_uint(f1)) {
-                    const uint32_t e = cos_sin_entry_call(f2);
-                    cv = (uint16_t)e;
-                    sv = (uint16_t)(e >> 16);
+            float a1[kAngIt], a2[kAngIt];
+#pragma unroll
+            for (int i = 0; i < kAngIt; ++i) {
+                const int64_t c = lane + 32 * i;
+                if (c < hh) {
+                    a1[i] = __ldg(fr + c);
+                    a2[i] = __ldg(fr + c + hh);
                 }
-                cs[w][0][c + hh] = cv;
-                cs[w][1][c + hh] = sv;
+            }
+#pragma unroll
+            for (int i = 0; i < kAngIt; ++i) {
+                const int64_t c = lane + 32 * i;
+                if (c < hh) {
+                    uint16_t cv, sv;
+                    cos_sin_entry(a1[i], cv, sv);
+                    cs[w][0][c] = cv;
+                    cs[w][1][c] = sv;
+                    if (__float_as_uint(a2[i]) != __float_as_uint(a1[i])) {
+                        const uint32_t e = cos_sin_entry_call(a2[i]);
+                        cv = (uint16_t)e;
+                        sv = (uint16_t)(e >> 16);
+                    }
+                    cs[w][0][c + hh] = cv;
+                    cs[w][1][c + hh] = sv;
+                }
             }
             __syncwarp();
             if (active && pair) {
