@@ -438,12 +438,17 @@ __global__ void __launch_bounds__(rms_max_threads(VPT), rms_min_blocks(VPT))
 // Narrow rows (at most 32 * VPT vectors): one warp per row, so the row's sum
 // needs shuffles only, no shared memory and no barrier; the warps of a CTA
 // work on different rows independently.  Persistent warps, each prefetching
-// its next row like the CTA-wide kernel, in CTAs of 4 warps.  Measured per
-// call at ~1.34 GB (32 * VPT a multiple of C / 8 or not): C = 768 225 us and
-// C = 1024 215 us against 288 and 277 us with a CTA per row.  The variant
-// without bounds checks for rows that fill the warp, and 8-warp CTAs, were
-// slower at some widths (C = 768: 452 us), so every width takes this one.
+// its next row like the CTA-wide kernel (up to 4 vectors per lane), in CTAs
+// of 4 warps.  Measured per call at ~1.34 GB (32 * VPT a multiple of C / 8 or
+// not): C = 768 225 us and C = 1024 215 us against 288 and 277 us with a CTA
+// per row; C = 1152 (5 vectors per lane, no prefetch) 241 against 346 us.
+// The variant without bounds checks for rows that fill the warp, and 8-warp
+// CTAs, were slower at some widths (C = 768: 452 us), so every width takes
+// this one.  From C = 1288 up a CTA per row is faster (C = 1536: 230 against
+// 249 us with 6 vectors per lane; C = 2048: 226 against 237 us).
 constexpr int kWarpRowThreads = 128;
+constexpr int kWarpPrefetchVpt = 4;  // up to this many vectors per lane, prefetch the next row
+constexpr int kWarpMaxVpt = 5;       // rows of up to 32 * 5 vectors (C <= 1280) take a warp
 
 template <int VPT>
 __global__ void __launch_bounds__(kWarpRowThreads) rms_warp_kernel(RmsParams p) {
@@ -453,6 +458,14 @@ __global__ void __launch_bounds__(kWarpRowThreads) rms_warp_kernel(RmsParams p) 
     uint4 wv[VPT], xc[VPT], rc[VPT];
     load_w<VPT, false, true>(p, nv, wv);
     int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if constexpr (VPT > kWarpPrefetchVpt) {
+        // wider rows: the row's own 2 * VPT loads per lane are enough in flight
+        for (; row < p.T; row += warps) {
+            load_row<VPT, false, true>(p, nv, row, xc, rc);
+            rms_row<VPT, false, true>(p, nullptr, 0, row, nv, xc, rc, wv);
+        }
+        return;
+    }
     if (row < p.T) load_row<VPT, false, true>(p, nv, row, xc, rc);
     for (; row < p.T; row += warps) {
         uint4 xn[VPT], rn[VPT];
@@ -550,14 +563,15 @@ cudaError_t launch_rmsnorm_residual(const RmsParams& p, cudaStream_t st) {
                      aligned(p.x, 16) && aligned(p.residual, 16) && aligned(p.w, 16) &&
                      aligned(p.out, 16);
     const int64_t nv = p.C / 8;
-    // rows of at most 128 vectors (C <= 1024): one warp per row, VPT = nv / 32
+    // rows of at most 160 vectors (C <= 1280): one warp per row, VPT = nv / 32
     // rounded up
-    if (vec && nv <= 4 * 32) {
+    if (vec && nv <= kWarpMaxVpt * 32) {
         switch ((nv + 31) / 32) {
             case 1: return launch_warp<1>(p, st);
             case 2: return launch_warp<2>(p, st);
             case 3: return launch_warp<3>(p, st);
-            default: return launch_warp<4>(p, st);
+            case 4: return launch_warp<4>(p, st);
+            default: return launch_warp<5>(p, st);
         }
     }
     // VPT vectors per thread: the smallest of 1, 2, 4 that keeps a row within

@@ -569,9 +569,10 @@ def test_rmsnorm_special_rows(C):
     _rms_check(x, r, w, None, "special rows")
 
 
-# Rows of at most 128 vectors of 8 take the one-warp-per-row kernel with 1-4
-# vectors per lane, filling the warp or not; 1032 is the first width past it.
-@pytest.mark.parametrize("C", [136, 264, 512, 520, 1000, 1024, 1032])
+# Rows of at most 160 vectors of 8 take the one-warp-per-row kernel with 1-5
+# vectors per lane (5 without the next-row prefetch), filling the warp or not;
+# 1288 is the first width past it.
+@pytest.mark.parametrize("C", [136, 264, 512, 520, 1000, 1024, 1032, 1152, 1280, 1288])
 def test_rmsnorm_warp_rows(C):
     T = 2053
     x = W.normal_bf16((T, C), 90 + C, 4)
