@@ -1,19 +1,24 @@
 """Benchmark of the DiT elementwise hot path on B300.
 
-One step = one pass of the whole path over one layer's synthetic tensors:
-  rope_cos_sin_precompute (the per-forward tables)
-  rope_rotate_half on q, rope_rotate_half on k
-  gelu_and_mul (GEGLU)
-  rmsnorm_residual twice (the pre-attention and pre-FFN norms of a Pre-Norm layer)
+One step = one pass of the whole path over one layer's synthetic tensors, in
+the order of a Pre-Norm layer:
+  the per-forward tables: rope_cos_sin_precompute and the GEGLU activation
+    table (on a side branch, beside the pre-attention norm)
+  rmsnorm_residual (pre-attention norm)
+  RoPE on q and k (one rope_rotate_half_qk launch; --rope separate: one
+    rope_rotate_half call per tensor)
+  rmsnorm_residual (pre-FFN norm)
+  gelu_and_mul (GEGLU, the streaming kernel on the table built above)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload video]
+                    [--rope qk|separate] [--serial]
     python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
 
 Prints one JSON line.  `value` is the aggregate algorithmic HBM throughput
 (GB/s: bytes each op must move, summed over the step and all ranks, over the
 device time of the K timed steps, max over ranks).  Inputs are resident in HBM
 before timing; every kernel's inputs exceed the 126 MB L2 except the cos/sin
-tables, which the step itself produces and the two RoPE calls consume.
+tables, which the step itself produces and its RoPE consumes.
 Multi-rank runs (torchrun) are independent replicas of the same layer (weak
 scaling); the path has no exchange step.
 """
