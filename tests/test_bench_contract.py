@@ -95,3 +95,28 @@ def test_sample_parity_checks_the_sampled_rows():
     diff = {n: o["differing"] for n, o in res["outputs"].items()}
     assert diff == {n: int(n == "cos") for n in layer.out_names}
     assert res["outputs"]["cos"]["max_ulp"] == 1
+
+
+def test_step_accounting_of_both_rope_forms():
+    """The step's calls and bytes: one q+k launch reads the tables once where two
+    rope_rotate_half calls read them twice; the GEGLU activation table is its own
+    launch; a sample of the whole layer counts the whole step."""
+    from diffusion_transformer_elementwise_rotate_b300 import workloads as W
+    wl = W.WORKLOADS["video"]
+    qk, sep = bench.step_ops("qk"), bench.step_ops("separate")
+    assert qk[:2] == list(bench.PER_FORWARD) and qk[-1] == bench.DOMINANT
+    assert qk == ["rope_cos_sin_precompute", "gelu_table_build", "rmsnorm_residual_attn",
+                  "rope_rotate_half_qk", "rmsnorm_residual_ffn", "gelu_and_mul"]
+    assert sep[3:5] == ["rope_rotate_half_q", "rope_rotate_half_k"] and len(sep) == len(qk) + 1
+    assert bench.launches_per_step("qk") == 6 and bench.launches_per_step("separate") == 7
+    bq, bs = bench.step_bytes(wl, W, "qk"), bench.step_bytes(wl, W, "separate")
+    assert list(bq) == qk and list(bs) == sep
+    tok = wl.B * wl.S
+    assert sum(bs.values()) - sum(bq.values()) == 4 * tok * wl.rot  # one more table read
+    assert bq["rope_rotate_half_qk"] == 2 * 4 * tok * wl.H * wl.D + 4 * tok * wl.rot
+    assert bq["gelu_table_build"] == 2 * 65536
+    whole = bench.sampled_bytes(bq, wl, wl.S, wl.T_ff, wl.T_norm)
+    assert whole == sum(bq.values())
+    half = bench.sampled_bytes(bq, wl, wl.S // 2, wl.T_ff // 2, wl.T_norm // 2)
+    assert abs(half - (sum(bq.values()) - bq["gelu_table_build"]) / 2
+               - bq["gelu_table_build"]) < 1e-3 * sum(bq.values())
