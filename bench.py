@@ -440,7 +440,7 @@ def timed_steps(dt, layer, steps, warm):
     return ms
 
 
-def other_workloads(dt, W, dev, steps, peak, rope="qk", serial=False):
+def other_workloads(dt, W, dev, steps, peak, rope="qk", serial=False, gpu_index=0):
     """The image and CFG layers: the same step on their shapes, timed like the
     headline layer (a pass of plain steps, then a pass with events between the
     kernels for the per-op figures), each on its own tensors.  Their steps move
@@ -452,8 +452,14 @@ def other_workloads(dt, W, dev, steps, peak, rope="qk", serial=False):
         layer = Layer(wl, W, dev, keep_host=False, rope=rope, serial=serial)
         bts = step_bytes(wl, W, rope)
         per_step = sum(bts.values())
+        # clocks over this layer's passes (graph capture included: the timed
+        # steps alone last a few milliseconds, under the sampling period)
+        sampler = ClockSampler(gpu_index)
+        sampler.start()
+        time.sleep(0.3)
         ms = timed_steps(dt, layer, steps, 3) / steps
         km = breakdown(dt, layer, steps)
+        clocks = sampler.stop()
         tokens = wl.B * wl.S
         res[name] = {
             "workload": config_for(wl, per_step, "replicas x1", rope)["workload"],
@@ -469,6 +475,7 @@ def other_workloads(dt, W, dev, steps, peak, rope="qk", serial=False):
                              "gbs": round(bts[op] / (km[op] / 1e3) / 1e9, 1),
                              "frac_of_hbm_peak": round(bts[op] / (km[op] / 1e3) / 1e9 / peak, 4)}
                         for op in layer.ops},
+            "clocks": clocks,
         }
         del layer
         torch.cuda.empty_cache()
@@ -883,7 +890,8 @@ def native(args):
     fused.update(geglu_prebuilt_table(dt, layer, wl, min(K, 200)))
 
     peak, peak_kind = peaks()
-    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak, args.rope, args.serial)
+    per_wl = other_workloads(dt, W, dev, max(20, min(K, 50)), peak, args.rope, args.serial,
+                             local)
     # the GEMM last: at the 1.1 kW power limit it leaves the GPU slower for a
     # while (memory-bound kernels timed right after it read 15-20% low)
     fused.update(fused_mlp_geglu(dt, layer, wl, max(3, min(K, 20))))
