@@ -13,17 +13,19 @@
 // the table kernel, hence the same bits) and never written to HBM.
 //
 // Fast path (hh = rot_dim / 2 and every stride and pointer a multiple of the
-// vector width VW, hh / VW <= 32, and rot_dim <= kMaxRot with angles):
+// vector width VW, at most 32 pair and tail items per head row, and
+// rot_dim <= kMaxRot with angles):
 //   - one warp per token (b, s); lanes own NP = hh / VW pair items (columns
 //     j..j+VW and j+hh..j+hh+VW) and walk the q rows and then the k rows,
 //     RPW = 32 / NP rows per pass, U rows per batch with all loads of a batch
 //     issued before any of its stores; the first batch is loaded before the
 //     token's cos/sin row is fetched or evaluated;
 //   - with angles, the warp first evaluates the token's rot_dim (cos, sin)
-//     pairs, one first-half column and its second-half partner per lane at a
-//     time (the partner's entry copied when its angle has the same bits),
-//     into its slot of shared memory and then reads its vectors from there;
-//     the same registers serve every q and k head of the token;
+//     pairs into its slot of shared memory: each lane loads the angles of its
+//     first-half columns and of their second-half partners, then evaluates
+//     them (a partner's entry copied when its angle has the same bits); the
+//     lanes then read their vectors from there, and the same registers serve
+//     every q and k head of the token;
 //   - tail columns [rot_dim, D) are not touched in place (they already hold
 //     x); out of place, NT = (D - rot_dim) / VW more items per head row copy
 //     them, so a lane's item is a pair (it < NP) or a tail vector, and NP + NT
