@@ -12,7 +12,9 @@
 // token row at a time: thread t owns the 8-column vectors k * blockDim + t of
 // every row (VPT of them), keeps its w vectors in registers for the whole
 // launch, and loads the next row's x and residual vectors into registers while
-// it works on the current one.  One HBM read of x and residual, one write of h
+// it works on the current one.  Rows of at most 1280 columns go to one warp
+// each instead (lane l owns the vectors k * 32 + l), so their sums need no
+// shared memory or barrier.  One HBM read of x and residual, one write of h
 // and out per row.  No fp64 on the common path (this part's fp64 rate is a
 // small fraction of its fp32 rate), so the row statistics are carried in fp32
 // pairs ("double-float", value = hi + lo):
@@ -20,7 +22,9 @@
 //   - sum of h^2: each square is exact in fp32 (a bf16 has 8 significant
 //     bits); accumulated with TwoSum on packed fp32x2 lanes, merged across the
 //     warp with shuffles and across warps through shared memory (every thread
-//     merges the warp partials in the same order, so all see the same total);
+//     merges the warp partials in the same order, so all see the same total;
+//     with a warp per row, the shuffle butterfly alone gives every lane the
+//     same total);
 //   - inv = (sum/C + eps)^(-1/2) as a double-float: rsqrtf seed plus one
 //     Newton step with an exactly computed residual (relative error ~2^-43);
 //   - out: h*w is exact in fp32; RN32(h*w*inv_hi) decides the bf16 rounding
