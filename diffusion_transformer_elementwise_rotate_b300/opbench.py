@@ -3,7 +3,7 @@ device: the standalone case behind the per-kernel DRAM-traffic captures and
 the per-launch timing spread.
 
     python -m diffusion_transformer_elementwise_rotate_b300.opbench --op OP
-        [--workload video] [--rows N] [--reps K] [--warmup W]
+        [--workload video] [--rows N] [--cols C] [--reps K] [--warmup W]
 
 OP is one of
   tables      rope_cos_sin_precompute on the workload's (S, B, 1, rot) angles
@@ -18,6 +18,8 @@ OP is one of
 
 --rows caps the op's row count (tokens for the RoPE ops, T for the others), so
 a capture can hold a slice of a layer that still exceeds the 126 MB L2.
+--cols sets the RMSNorm width C (and, with --rows, its row count exactly), for
+widths no workload has (the one-warp-per-row kernel takes C <= 1280).
 Inputs are drawn on the device (torch's CUDA generator, seed 0) with the
 workload's distributions: timing does not depend on the values, and drawing a
 few GB on the host would dominate a short run.  Every launch is bracketed by
@@ -48,7 +50,7 @@ def _normal(shape, dev, g, mean=0.0, std=1.0):
     return t.to(torch.bfloat16)
 
 
-def setup(op: str, wl: W.Workload, rows: int | None, dev):
+def setup(op: str, wl: W.Workload, rows: int | None, dev, cols: int | None = None):
     """(callable running one launch of the op, algorithmic bytes or flops, unit,
     description, live tensors)."""
     g = torch.Generator(device=dev).manual_seed(0)
@@ -97,8 +99,8 @@ def setup(op: str, wl: W.Workload, rows: int | None, dev):
         return (lambda: dt.gelu_and_mul(gu[:, :F], gu[:, F:], out=out, table=tab), 6 * T * F,
                 "B", f"gelu_and_mul ({T}, 2x{F}), prebuilt activation table", (gu, out, tab))
     if op == "rmsnorm":
-        T = wl.T_norm if rows is None else min(wl.T_norm, rows)
-        C = wl.C
+        T = wl.T_norm if rows is None else (rows if cols else min(wl.T_norm, rows))
+        C = wl.C if cols is None else cols
         x = _normal((T, C), dev, g)
         r = _normal((T, C), dev, g, std=2.0)
         w = _normal((C,), dev, g, mean=1.0, std=math.sqrt(0.1))
@@ -138,13 +140,13 @@ def _graph(fn, n, evs=None):
 
 
 def run(op: str, workload: str = "video", rows: int | None = None, reps: int = 20,
-        warmup: int = 3, graph: bool = True) -> dict:
+        warmup: int = 3, graph: bool = True, cols: int | None = None) -> dict:
     """Per-launch times (events around each call) and the back-to-back rate
     (reps calls between two events).  With graph=True both run as CUDA graphs,
     so that host launch overhead never shows in the times (a short kernel
     launched from Python one call at a time can leave the GPU waiting)."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    fn, work, unit, desc, _live = setup(op, W.WORKLOADS[workload], rows, dev)
+    fn, work, unit, desc, _live = setup(op, W.WORKLOADS[workload], rows, dev, cols)
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -186,12 +188,16 @@ def main():
     ap.add_argument("--op", required=True, choices=OPS)
     ap.add_argument("--workload", default="video", choices=sorted(W.WORKLOADS))
     ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--cols", type=int, default=None, help="RMSNorm width C")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--eager", action="store_true",
                     help="launch from Python one call at a time instead of CUDA graphs")
     a = ap.parse_args()
-    print(json.dumps(run(a.op, a.workload, a.rows, a.reps, a.warmup, not a.eager)), flush=True)
+    if a.cols is not None and a.op != "rmsnorm":
+        ap.error("--cols applies to --op rmsnorm only")
+    print(json.dumps(run(a.op, a.workload, a.rows, a.reps, a.warmup, not a.eager, a.cols)),
+          flush=True)
 
 
 if __name__ == "__main__":
