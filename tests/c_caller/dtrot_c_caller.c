@@ -85,12 +85,14 @@ int main(int argc, char** argv) {
     uint16_t* hx = (uint16_t*)to_device(read_file(dir, "hx.bf16", nn * 2), nn * 2);
     uint16_t* hr = (uint16_t*)to_device(read_file(dir, "hr.bf16", nn * 2), nn * 2);
     uint16_t* hw = (uint16_t*)to_device(read_file(dir, "hw.bf16", (size_t)C * 2), (size_t)C * 2);
-    uint16_t *cs, *sn, *out, *ff, *ff2, *y;
+    uint16_t *cs, *sn, *out, *qo, *ko, *ff, *ff2, *y;
     void* ws;
     const int64_t wsb = dtrot_gelu_and_mul_workspace_bytes();
     CUDA(cudaMalloc((void**)&cs, nt * 2));
     CUDA(cudaMalloc((void**)&sn, nt * 2));
     CUDA(cudaMalloc((void**)&out, nx * 2));
+    CUDA(cudaMalloc((void**)&qo, nx * 2));
+    CUDA(cudaMalloc((void**)&ko, nx * 2));
     CUDA(cudaMalloc((void**)&ff, no * 2));
     CUDA(cudaMalloc((void**)&ff2, no * 2));
     CUDA(cudaMalloc((void**)&y, nn * 2));
@@ -100,6 +102,10 @@ int main(int argc, char** argv) {
     DTROT(dtrot_rope_cos_sin_precompute(freqs, S, B, R, cs, sn, NULL));
     DTROT(dtrot_rope_rotate_half(x, B, S, H, D, S * H * D, H * D, D, cs, sn, R, out, S * H * D,
                                  H * D, D, NULL));
+    /* q and k in one out-of-place launch; both read x (inputs may overlap) */
+    DTROT(dtrot_rope_rotate_half_qk_out(x, H, S * H * D, H * D, D, x, H, S * H * D, H * D, D, B,
+                                        S, D, cs, sn, NULL, R, qo, S * H * D, H * D, D, ko,
+                                        S * H * D, H * D, D, NULL));
     DTROT(dtrot_gelu_and_mul(gu, 2 * F, gu + F, 2 * F, ff, F, T, F, ws, wsb, NULL));
     DTROT(dtrot_gelu_and_mul_noalloc(gu, 2 * F, gu + F, 2 * F, ff2, F, T, F, NULL));
     DTROT(dtrot_rmsnorm_residual(hx, C, hr, C, hw, 1e-6f, y, C, T, C, NULL));
@@ -114,6 +120,8 @@ int main(int argc, char** argv) {
     from_device(dir, "cos.bf16", cs, nt * 2);
     from_device(dir, "sin.bf16", sn, nt * 2);
     from_device(dir, "rope.bf16", out, nx * 2);
+    from_device(dir, "rope_qk_q.bf16", qo, nx * 2);
+    from_device(dir, "rope_qk_k.bf16", ko, nx * 2);
     from_device(dir, "geglu.bf16", ff, no * 2);
     from_device(dir, "geglu_noalloc.bf16", ff2, no * 2);
     from_device(dir, "residual.bf16", hr, nn * 2);

@@ -71,6 +71,8 @@ def test_plain_c_caller_matches_the_oracle(tmp_path):
     assert_bitexact(load("cos.bf16", ec.shape), ec, "cos")
     assert_bitexact(load("sin.bf16", es.shape), es, "sin")
     assert_bitexact(load("rope.bf16", x.shape), oracle.rope_rotate_half(x, ec, es), "rope")
+    for n in ("rope_qk_q.bf16", "rope_qk_k.bf16"):  # one out-of-place q+k launch, tail copied
+        assert_bitexact(load(n, x.shape), oracle.rope_rotate_half(x, ec, es), n)
     ref = oracle.gelu_and_mul(gu[:, :F], gu[:, F:])
     assert_within_tolerance(load("geglu.bf16", (T, F)), ref, "geglu")
     assert_bitexact(load("geglu_noalloc.bf16", (T, F)), load("geglu.bf16", (T, F)),
